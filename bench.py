@@ -1,0 +1,379 @@
+"""Benchmark of the DFlash 2 path selector on GB300.
+
+One step = one pass of the whole selector (lm_head + top-K, merge,
+projections, pair tables + walk) and the greedy accept check over one batch
+of seeded synthetic inputs already resident in HBM. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4b_b1]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (the selector has no cross-sequence exchange); the
+time is the max over ranks and rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "selector draft blocks/s and achieved HBM GB/s (fraction of GB300 roofline)"
+UNIT = "blocks/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "lmhead_topk_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="4b_b1")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_src_digest():
+    h = hashlib.sha256()
+    for f in ("lmhead_topk.cu", "common.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "speculative_decoding_draft_tcgen05_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def committed_traffic(workload):
+    """DRAM bytes per launch of the lm_head kernel from a committed ncu capture,
+    if the kernel source is unchanged since (else None)."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        if t.get("kernel_src_sha256") != kernel_src_digest():
+            return None
+        return t["per_launch_bytes"].get(workload)
+    except Exception:
+        return None
+
+
+def algorithmic_bytes(w, G, N):
+    """Bytes the selector must move per step (see the design notes): the whole
+    path and, separately, the lm_head+top-K kernel."""
+    d, V, L, K, B, e = w.d, w.V, w.L, w.K, w.B, w.e
+    k1 = (V * d * 2            # lm_head weight, read once
+          + e * d * 2          # W_H (the gate rows share the pass)
+          + N * d * 2          # hidden states
+          + G * N * K * 8      # partial top-K lists written
+          + N * e * 4)         # gate g written
+    R = L * K + 1
+    rest = (G * N * K * 8      # partial lists read by the merge
+            + N * K * 8        # merged ids + values
+            + B * R * d * 2    # gathered E rows
+            + 2 * e * d * 2    # W_A, W_B
+            + B * R * 2 * e * 4 * 2  # projections written and read
+            + N * e * 4        # gate read
+            + N * K * K * 4    # pair tables written
+            + B * (L + 1) * 4 + B * L * 4 * 2 + B * 4 + B * (L + 1) * 4)  # path, target, accept, emitted
+    return k1, k1 + rest
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu_id)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(inp, seconds):
+    """The oracle, as it is, on the host cores: whole blocks of the workload
+    (one sequence each), repeated for about `seconds`."""
+    import oracle
+    from speculative_decoding_draft_tcgen05_gb300 import workloads as wl
+    b = wl.bf16_bits
+    Wb, Eb, WAb, WBb, WHb = b(inp.W), b(inp.E), b(inp.W_A), b(inp.W_B), b(inp.W_H)
+    cores = len(os.sched_getaffinity(0))
+    n, t0 = 0, time.perf_counter()
+    while True:
+        s = n % inp.wl.B
+        oracle.select(Wb, Eb, WAb, WBb, WHb, b(inp.hidden[s]), int(inp.anchor[s]), inp.wl.K, nthreads=cores)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": n / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} whole blocks (one sequence each) of the {inp.wl.name} workload through the fp64 C "
+                      f"oracle with OpenMP over {cores} threads, {el:.1f} s"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is one block of the
+    workload through the oracle on a slice of the vocabulary sized so the whole
+    run stays within a few minutes; the time is scaled to the full vocabulary."""
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from speculative_decoding_draft_tcgen05_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w)
+    b = wl.bf16_bits
+    cores = len(os.sched_getaffinity(0))
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    # calibrate: time per vocabulary row of one block
+    Vs = min(w.V, 8192)
+    t0 = time.perf_counter()
+    oracle.select(b(inp.W[:Vs]), b(inp.E), b(inp.W_A), b(inp.W_B), b(inp.W_H), b(inp.hidden[0]),
+                  int(inp.anchor[0]), w.K, nthreads=cores)
+    per_row = (time.perf_counter() - t0) / Vs
+    Vs = int(max(w.K + 1, min(w.V, budget / per_row)))
+    Wb, Eb, WAb, WBb, WHb = b(inp.W[:Vs]), b(inp.E), b(inp.W_A), b(inp.W_B), b(inp.W_H)
+    anchors = [int(a) % Vs for a in inp.anchor.tolist()]
+    for i in range(args.warmup):
+        s = i % w.B
+        oracle.select(Wb, Eb, WAb, WBb, WHb, b(inp.hidden[s]), anchors[s], w.K, nthreads=cores)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s = i % w.B
+        oracle.select(Wb, Eb, WAb, WBb, WHb, b(inp.hidden[s]), anchors[s], w.K, nthreads=cores)
+    el = time.perf_counter() - t0
+    scale = w.V / Vs
+    per_block = el / max(1, args.steps) * scale
+    value = 1.0 / per_block
+    sample = (f"each step: one block (one sequence, L={w.L}) of the {w.name} workload through the fp64 C oracle "
+              f"with the vocabulary cut to its first {Vs} of {w.V} rows; time scaled by {scale:.2f} to the full "
+              f"vocabulary; OpenMP over {cores} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_block * 1e3 * w.B,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.label, "B": w.B, "L": w.L, "K": w.K, "V": w.V, "d": w.d},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import speculative_decoding_draft_tcgen05_gb300 as pkg
+    from speculative_decoding_draft_tcgen05_gb300 import build as pbuild
+    from speculative_decoding_draft_tcgen05_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    pbuild.build()
+    pkg.lib()
+
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.make_inputs(w)
+    W, E, WA, WB, WH = (x.to(dev) for x in (inp.W, inp.E, inp.W_A, inp.W_B, inp.W_H))
+    hidden = inp.hidden.to(dev)
+    anchor = inp.anchor.to(dev)
+    stream = torch.cuda.Stream(dev)
+    sel = pkg.Selector(W, E, WA, WB, WH, L=w.L, K=w.K, max_batch=w.B)
+    out = sel.outputs(w.B, full=False)
+    accept = torch.empty(w.B, dtype=torch.int32, device=dev)
+    emitted = torch.empty(w.B, w.L + 1, dtype=torch.int32, device=dev)
+
+    # target tokens: planted on the selector's own path from an untimed run
+    # (they only set how long the accepted prefixes are)
+    with torch.cuda.stream(stream):
+        pkg.dflash_select_run(sel.h, hidden, anchor, stream=stream, **out)
+    stream.synchronize()
+    target = wl.plant_targets(out["path"].cpu(), inp.target_rand, inp.n0, w.V).to(dev)
+
+    def step():
+        pkg.dflash_select_run(sel.h, hidden, anchor, stream=stream, **out)
+        pkg.dflash_verify_prefix(out["path"], target, accept, emitted, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    pkg.dflash_select_sync_status(sel.h, stream=stream)
+
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else (gpu_id or local)
+    clocks = ClockSampler(gpu_id)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    pkg.dflash_select_profile(sel.h, True)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler attach before the timed region
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1)
+    prof = pkg.dflash_select_profile_read(sel.h)
+    pkg.dflash_select_profile(sel.h, False)
+    pkg.dflash_select_sync_status(sel.h, stream=stream)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end through the host-buffer entry point: pinned inputs in, results out, every step
+    hid_h = inp.hidden.pin_memory()
+    anc_h = inp.anchor.pin_memory()
+    tgt_h = target.cpu().pin_memory()
+    path_h = torch.empty(w.B, w.L, dtype=torch.int32).pin_memory()
+    acc_h = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    em_h = torch.empty(w.B, w.L + 1, dtype=torch.int32).pin_memory()
+    for _ in range(10):
+        pkg.dflash_select_step_host(sel.h, hid_h, anc_h, tgt_h, path_h, acc_h, em_h, stream=stream)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        pkg.dflash_select_step_host(sel.h, hid_h, anc_h, tgt_h, path_h, acc_h, em_h, stream=stream)
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = hid_h.numel() * 2 + anc_h.numel() * 4 + tgt_h.numel() * 4
+    d2h = path_h.numel() * 4 + acc_h.numel() * 4 + em_h.numel() * 4 + 4
+
+    launches_per_step = pkg.dflash_select_launches_per_run(sel.h, w.B) + 1
+    N = w.B * w.L
+    NT = ((N + 15) // 16) * 16 if N <= 256 else 256
+    n_tiles = math.ceil(N / NT)
+    m_total = math.ceil(w.V / 128) + 2
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    G = max(1, min(m_total, sms // n_tiles))
+    k1_bytes, all_bytes = algorithmic_bytes(w, G, N)
+    k1_ms, k1_n = prof["lmhead_topk"]
+    k1_avg_s = k1_ms / max(1, k1_n) / 1e3
+    peak, peak_kind = hbm_peak()
+    achieved = k1_bytes / k1_avg_s / 1e9
+    step_s = ms / 1e3 / args.steps
+    value = world * w.B / step_s
+    sel.close()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.label, "B": w.B, "L": w.L, "K": w.K, "V": w.V, "d": w.d, "e": w.e,
+                       "seed": w.seed, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (lm_head weight %.0f MB > 129 MB L2), no flush" % (w.V * w.d * 2 / 1e6)},
+            "hbm_gbs_step": all_bytes / step_s / 1e9,
+            "hbm_frac_step": all_bytes / step_s / 1e9 / peak,
+            "roofline": {"bound": "hbm", "kernel": "lmhead_topk", "achieved": achieved, "peak": peak,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback 6.8 TB/s", "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": committed_traffic(args.workload),
+                         "algorithmic_bytes_per_launch": k1_bytes, "avg_launch_us": k1_avg_s * 1e6,
+                         "launches_timed": k1_n},
+            "kernels_avg_us": {k: v[0] / max(1, v[1]) * 1e3 for k, v in prof.items()},
+            "clocks": clk,
+            "e2e": {"value": world * w.B * args.e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                    "api": "dflash_select_step_host (pinned host buffers, copies and sync inside)"},
+            "gpu_launches": launches_per_step * args.steps,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(inp, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,159 @@
+/*
+ * dflash_select.h — C ABI of the DFlash 2 path selector on one GB300 GPU.
+ *
+ * The path selector sits between DFlash 2's one-pass block drafter and the
+ * target model's verification pass (blog post "DFlash 2: Keep Drafting
+ * Parallel", section "A Lightweight Path Selector"). For every sequence of a
+ * batch and every draft position t of its block it
+ *   1. forms the drafter's lm_head logits U_t = W h_t and keeps the K best
+ *      tokens (section "The Right Tokens Are Already There": the right token
+ *      is usually among the top 16);
+ *   2. scores every adjacent candidate pair,
+ *        S_t(a, b) = U_t(b) + < A(a) (.) H(h_t), B(b) >,
+ *      with A(a) = W_A E[a], B(b) = W_B E[b], H(h) = W_H h (the pages do not
+ *      say how A, B and H are parameterised; this library takes one shared
+ *      token table E [V, d] and three [256, d] projections);
+ *   3. walks the precomputed tables from the last verified token x0 and
+ *      emits one draft path (max-sum walk by default; the literal
+ *      best-successor walk on request);
+ *   4. (dflash_verify_prefix) keeps the longest prefix of that path that
+ *      equals the target's argmax tokens, plus the target's next token.
+ *
+ * Conventions of every entry point:
+ *   - Tensor arguments are DEVICE pointers owned by the caller, row-major and
+ *     densely packed, unless the name ends in _host. bf16 is IEEE bfloat16
+ *     stored as 16-bit words.
+ *   - Calls are asynchronous and ordered on the CUDA stream given as
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream). Output
+ *     buffers are valid once the stream reaches the point of the call.
+ *   - The library never aborts and never exits. A non-zero dflash_status
+ *     means nothing was launched; dflash_last_error() then returns a
+ *     thread-local message. Problems that only the GPU can see (a token id
+ *     out of [0, V), a pipeline wait that ran out of time) are latched in a
+ *     device error word that dflash_select_sync_status() reports.
+ *   - Draft positions are numbered t = 0 .. L-1 (the pages' positions
+ *     1 .. L); x0 precedes position 0.
+ */
+#ifndef DFLASH_SELECT_H
+#define DFLASH_SELECT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DFLASH_OK = 0,
+    DFLASH_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer */
+    DFLASH_ERR_UNSUPPORTED = 2,   /* shape outside the supported set, or not an sm_103 GPU */
+    DFLASH_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    DFLASH_ERR_DEVICE_CHECK = 4,  /* a kernel saw an out-of-range token id */
+    DFLASH_ERR_TIMEOUT = 5        /* a kernel pipeline wait exceeded its bound */
+} dflash_status;
+
+typedef enum {
+    DFLASH_WALK_VITERBI = 0,  /* max-sum walk over the pair tables */
+    DFLASH_WALK_GREEDY = 1    /* from x0, follow the best successor at each step */
+} dflash_walk;
+
+/* Shapes fixed for the lifetime of a handle.
+ * Supported: 1 <= L <= 16; K in {16, 32}; K <= V; d % 64 == 0, 64 <= d <= 16384;
+ * e == 256; 1 <= max_batch with max_batch * L <= 8192; V < 2^31. */
+typedef struct {
+    int64_t V;          /* vocabulary size (rows of W and E) */
+    int32_t d;          /* drafter hidden width */
+    int32_t L;          /* draft positions per block (block size - 1) */
+    int32_t K;          /* candidates kept per position */
+    int32_t e;          /* width of A, B and H; must be 256 */
+    int32_t max_batch;  /* largest batch any run will pass; sizes the workspace */
+    int32_t walk;       /* dflash_walk */
+    float tie_eps;      /* margin under which tie_flags are raised, e.g. 1e-3 */
+} dflash_select_config;
+
+typedef struct dflash_select_ctx *dflash_select_handle;
+
+/* Creates a selector for the weights below (blog, "A Lightweight Path
+ * Selector": U_t from the drafter's own lm_head, A/B/H of width 256).
+ *   W_lm [V, d] bf16  lm_head weight        E   [V, d] bf16 token table
+ *   W_A, W_B, W_H [e, d] bf16               (all 16-byte aligned)
+ * The weights are borrowed, not copied: they must stay valid and unchanged
+ * until dflash_select_destroy. The handle owns a device workspace sized for
+ * cfg->max_batch, allocated here (the only allocation the selector makes).
+ * `stream` orders the workspace initialisation. Errors: INVALID_ARG,
+ * UNSUPPORTED, CUDA. */
+dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_lm, const void *E,
+                                 const void *W_A, const void *W_B, const void *W_H, void *stream,
+                                 dflash_select_handle *out);
+
+/* Runs the selector on B sequences (0 <= B <= max_batch; B == 0 is a no-op).
+ *   hidden     [B, L, d] bf16  drafter's final hidden states (16-byte aligned)
+ *   anchor     [B] int32       last verified token x0 of each sequence
+ * Outputs (NULL = not wanted, except path):
+ *   topk_ids   [B, L, K] int32 candidates, by logit descending then id ascending
+ *   topk_vals  [B, L, K] fp32  their logits U_t
+ *   pair_scores[B, L, K, K] fp32  S_t(candidate i of t-1, candidate j of t);
+ *              at t = 0 row 0 holds S_0(x0, j) and rows 1..K-1 are -inf
+ *   path       [B, L] int32    emitted draft tokens
+ *   path_score [B] fp32        sum of the path's pair scores
+ *   tie_flags  [B, L] uint8    bit 0: the walk's choice at t had a margin
+ *              below tie_eps; bit 1 (t = L-1 only): the final choice did
+ * Errors: INVALID_ARG (bad handle, B, pointer or alignment), CUDA. */
+dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, const int32_t *anchor,
+                                int32_t B, int32_t *topk_ids, float *topk_vals, float *pair_scores,
+                                int32_t *path, float *path_score, uint8_t *tie_flags, void *stream);
+
+/* Greedy verification (blog intro: the target checks the whole block in one
+ * pass and keeps the right guesses; the dev.to commentary: greedy output
+ * matches the target exactly).
+ *   path      [B, L] int32    draft tokens
+ *   target    [B, L+1] int32  target argmax token after x0, path[0], ..., path[L-1]
+ *   accept_len[B] int32       n = number of leading t with path[t] == target[t]
+ *   emitted   [B, L+1] int32  path[0..n-1], target[n], then -1 (NULL = not wanted)
+ * 0 <= B, 1 <= L <= 16. Needs no handle. Errors: INVALID_ARG, CUDA. */
+dflash_status dflash_verify_prefix(const int32_t *path, const int32_t *target, int32_t B, int32_t L,
+                                   int32_t *accept_len, int32_t *emitted, void *stream);
+
+/* One whole draft-verify step from HOST buffers: copies hidden/anchor/target
+ * to the handle's device staging area, runs dflash_select_run and
+ * dflash_verify_prefix, copies path, accept_len and emitted back, and waits
+ * for the stream. Host buffers should be pinned for asynchronous copies.
+ *   hidden_host [B, L, d] bf16, anchor_host [B], target_host [B, L+1] int32
+ *   path_host [B, L], accept_host [B], emitted_host [B, L+1] int32 (outputs)
+ * Returns the same errors as the two calls, and any latched device error. */
+dflash_status dflash_select_step_host(dflash_select_handle h, const void *hidden_host,
+                                      const int32_t *anchor_host, const int32_t *target_host,
+                                      int32_t B, int32_t *path_host, int32_t *accept_host,
+                                      int32_t *emitted_host, void *stream);
+
+/* Waits for `stream`, then reports and clears the handle's device error word:
+ * DFLASH_OK, DFLASH_ERR_DEVICE_CHECK or DFLASH_ERR_TIMEOUT. */
+dflash_status dflash_select_sync_status(dflash_select_handle h, void *stream);
+
+/* Per-kernel timing of later runs with CUDA events on the run's stream
+ * (enable = 1 turns it on and clears the record, 0 turns it off). */
+dflash_status dflash_select_profile(dflash_select_handle h, int32_t enable);
+
+/* Reads the record: for kernel index k (0 = lm_head+top-K, 1 = merge,
+ * 2 = projection, 3 = pair tables + walk), total milliseconds and launch
+ * count over the recorded runs (at most 4096 runs are recorded). Waits for
+ * the recorded events. n_kernels receives the number of kernel indices. */
+dflash_status dflash_select_profile_read(dflash_select_handle h, double *ms_total,
+                                         int64_t *launches, int32_t max_kernels,
+                                         int32_t *n_kernels);
+
+/* Number of kernel launches one dflash_select_run makes for batch B. */
+int32_t dflash_select_launches_per_run(dflash_select_handle h, int32_t B);
+
+/* Frees the workspace (after the device is idle) and the handle. Returns a
+ * latched device error if one is pending, else DFLASH_OK. NULL is a no-op. */
+dflash_status dflash_select_destroy(dflash_select_handle h);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *dflash_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_SELECT_H */

@@ -1,0 +1,228 @@
+"""DFlash 2 path selector on one GB300 GPU: Python binding of libdflash_select.
+
+The functions below have the names of the C entry points declared in
+``include/dflash_select.h`` and only marshal arguments: every step of the
+selector runs in the library's CUDA kernels. PyTorch supplies device memory
+and streams. If the library has not been built the calls raise; there is no
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libdflash_select.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "dflash_select.h")
+
+DFLASH_OK = 0
+DFLASH_ERR_INVALID_ARG = 1
+DFLASH_ERR_UNSUPPORTED = 2
+DFLASH_ERR_CUDA = 3
+DFLASH_ERR_DEVICE_CHECK = 4
+DFLASH_ERR_TIMEOUT = 5
+STATUS_NAMES = {0: "DFLASH_OK", 1: "DFLASH_ERR_INVALID_ARG", 2: "DFLASH_ERR_UNSUPPORTED", 3: "DFLASH_ERR_CUDA",
+                4: "DFLASH_ERR_DEVICE_CHECK", 5: "DFLASH_ERR_TIMEOUT"}
+
+DFLASH_WALK_VITERBI = 0
+DFLASH_WALK_GREEDY = 1
+
+KERNEL_NAMES = ("lmhead_topk", "topk_merge", "projection", "pair_walk")
+
+
+class DflashError(RuntimeError):
+    def __init__(self, status: int, func: str, msg: str):
+        super().__init__(f"{func}: {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class dflash_select_config(ctypes.Structure):
+    _fields_ = [("V", ctypes.c_int64), ("d", ctypes.c_int32), ("L", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("e", ctypes.c_int32), ("max_batch", ctypes.c_int32), ("walk", ctypes.c_int32),
+                ("tie_eps", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it first (python -m "
+                                   "speculative_decoding_draft_tcgen05_gb300.build)")
+            L = ctypes.CDLL(LIB_PATH)
+            P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            L.dflash_select_init.argtypes = [ctypes.POINTER(dflash_select_config), P, P, P, P, P, P,
+                                             ctypes.POINTER(P)]
+            L.dflash_select_run.argtypes = [P, P, P, i32, P, P, P, P, P, P, P]
+            L.dflash_verify_prefix.argtypes = [P, P, i32, i32, P, P, P]
+            L.dflash_select_step_host.argtypes = [P, P, P, P, i32, P, P, P, P]
+            L.dflash_select_sync_status.argtypes = [P, P]
+            L.dflash_select_profile.argtypes = [P, i32]
+            L.dflash_select_profile_read.argtypes = [P, P, P, i32, P]
+            L.dflash_select_launches_per_run.argtypes = [P, i32]
+            L.dflash_select_launches_per_run.restype = i32
+            L.dflash_select_destroy.argtypes = [P]
+            L.dflash_last_error.restype = ctypes.c_char_p
+            for f in ("dflash_select_init", "dflash_select_run", "dflash_verify_prefix", "dflash_select_step_host",
+                      "dflash_select_sync_status", "dflash_select_profile", "dflash_select_profile_read",
+                      "dflash_select_destroy"):
+                getattr(L, f).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def dflash_last_error() -> str:
+    return lib().dflash_last_error().decode(errors="replace")
+
+
+def _check(status: int, func: str):
+    if status != DFLASH_OK:
+        raise DflashError(status, func, dflash_last_error())
+
+
+def _ptr(t, dtype=None, name="tensor", device=True):
+    """Device (or host) address of a contiguous tensor; None stays NULL."""
+    if t is None:
+        return None
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not device and t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def dflash_select_init(W, E, W_A, W_B, W_H, *, L: int, K: int, max_batch: int, walk: int = DFLASH_WALK_VITERBI,
+                       tie_eps: float = 1e-3, stream=None):
+    """Creates a selector handle over device bf16 weights W [V, d], E [V, d], W_A/W_B/W_H [256, d]."""
+    import torch
+    V, d = W.shape
+    cfg = dflash_select_config(V=V, d=d, L=L, K=K, e=W_A.shape[0], max_batch=max_batch, walk=walk,
+                               tie_eps=tie_eps)
+    h = ctypes.c_void_p()
+    _check(lib().dflash_select_init(ctypes.byref(cfg), _ptr(W, torch.bfloat16, "W"), _ptr(E, torch.bfloat16, "E"),
+                                    _ptr(W_A, torch.bfloat16, "W_A"), _ptr(W_B, torch.bfloat16, "W_B"),
+                                    _ptr(W_H, torch.bfloat16, "W_H"), _stream(stream), ctypes.byref(h)),
+           "dflash_select_init")
+    return h
+
+
+def dflash_select_run(handle, hidden, anchor, *, path, topk_ids=None, topk_vals=None, pair_scores=None,
+                      path_score=None, tie_flags=None, stream=None):
+    """Runs the selector for hidden [B, L, d] bf16 and anchor [B] int32 into the given device outputs."""
+    import torch
+    B = anchor.shape[0]
+    _check(lib().dflash_select_run(handle, _ptr(hidden, torch.bfloat16, "hidden"), _ptr(anchor, torch.int32, "anchor"),
+                                   B, _ptr(topk_ids, torch.int32, "topk_ids"),
+                                   _ptr(topk_vals, torch.float32, "topk_vals"),
+                                   _ptr(pair_scores, torch.float32, "pair_scores"), _ptr(path, torch.int32, "path"),
+                                   _ptr(path_score, torch.float32, "path_score"),
+                                   _ptr(tie_flags, torch.uint8, "tie_flags"), _stream(stream)), "dflash_select_run")
+
+
+def dflash_verify_prefix(path, target, accept_len, emitted=None, stream=None):
+    """Greedy accept lengths of path [B, L] against target [B, L+1] (int32, device)."""
+    import torch
+    B, L = path.shape
+    _check(lib().dflash_verify_prefix(_ptr(path, torch.int32, "path"), _ptr(target, torch.int32, "target"), B, L,
+                                      _ptr(accept_len, torch.int32, "accept_len"),
+                                      _ptr(emitted, torch.int32, "emitted"), _stream(stream)), "dflash_verify_prefix")
+
+
+def dflash_select_step_host(handle, hidden_host, anchor_host, target_host, path_host, accept_host, emitted_host,
+                            stream=None):
+    """Whole step from host buffers (pinned for asynchronous copies); returns when results are on the host."""
+    import torch
+    B = anchor_host.shape[0]
+    _check(lib().dflash_select_step_host(handle, _ptr(hidden_host, torch.bfloat16, "hidden_host", device=False),
+                                         _ptr(anchor_host, torch.int32, "anchor_host", device=False),
+                                         _ptr(target_host, torch.int32, "target_host", device=False), B,
+                                         _ptr(path_host, torch.int32, "path_host", device=False),
+                                         _ptr(accept_host, torch.int32, "accept_host", device=False),
+                                         _ptr(emitted_host, torch.int32, "emitted_host", device=False),
+                                         _stream(stream)), "dflash_select_step_host")
+
+
+def dflash_select_sync_status(handle, stream=None) -> int:
+    """Waits for the stream; returns the latched device status (raises on error)."""
+    st = lib().dflash_select_sync_status(handle, _stream(stream))
+    _check(st, "dflash_select_sync_status")
+    return st
+
+
+def dflash_select_profile(handle, enable: bool):
+    _check(lib().dflash_select_profile(handle, int(bool(enable))), "dflash_select_profile")
+
+
+def dflash_select_profile_read(handle):
+    """{kernel name: (total ms, launches)} over the recorded runs."""
+    n = len(KERNEL_NAMES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    nk = ctypes.c_int32()
+    _check(lib().dflash_select_profile_read(handle, ms, cnt, n, ctypes.byref(nk)), "dflash_select_profile_read")
+    return {KERNEL_NAMES[i]: (ms[i], cnt[i]) for i in range(nk.value)}
+
+
+def dflash_select_launches_per_run(handle, B: int) -> int:
+    return int(lib().dflash_select_launches_per_run(handle, B))
+
+
+def dflash_select_destroy(handle):
+    _check(lib().dflash_select_destroy(handle), "dflash_select_destroy")
+
+
+class Selector:
+    """Owns a handle and the output tensors of one batch size (convenience only)."""
+
+    def __init__(self, W, E, W_A, W_B, W_H, *, L, K, max_batch, walk=DFLASH_WALK_VITERBI, tie_eps=1e-3):
+        import torch
+        self.L, self.K, self.max_batch = L, K, max_batch
+        self.device = W.device
+        self.h = dflash_select_init(W, E, W_A, W_B, W_H, L=L, K=K, max_batch=max_batch, walk=walk, tie_eps=tie_eps)
+        self._torch = torch
+
+    def outputs(self, B, full=True):
+        t = self._torch
+        dev = self.device
+        out = dict(path=t.empty(B, self.L, dtype=t.int32, device=dev))
+        if full:
+            out.update(topk_ids=t.empty(B, self.L, self.K, dtype=t.int32, device=dev),
+                       topk_vals=t.empty(B, self.L, self.K, dtype=t.float32, device=dev),
+                       pair_scores=t.empty(B, self.L, self.K, self.K, dtype=t.float32, device=dev),
+                       path_score=t.empty(B, dtype=t.float32, device=dev),
+                       tie_flags=t.empty(B, self.L, dtype=t.uint8, device=dev))
+        return out
+
+    def run(self, hidden, anchor, out=None, stream=None):
+        if out is None:
+            out = self.outputs(anchor.shape[0])
+        dflash_select_run(self.h, hidden, anchor, stream=stream, **out)
+        return out
+
+    def close(self):
+        if self.h is not None:
+            dflash_select_destroy(self.h)
+            self.h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

@@ -1,0 +1,494 @@
+// Host side of the C ABI declared in include/dflash_select.h: argument
+// validation, the device workspace, TMA descriptors, the launch sequence of
+// one selector run, and per-kernel event timing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "dflash_select.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+dflash_status fail(dflash_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+dflash_status ok()
+{
+    return DFLASH_OK;
+}
+
+#define CUDA_TRY(call)                                                                                    \
+    do {                                                                                                  \
+        cudaError_t e_ = (call);                                                                          \
+        if (e_ != cudaSuccess)                                                                            \
+            return fail(DFLASH_ERR_CUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, \
+                        __LINE__);                                                                        \
+    } while (0)
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// bf16 [rows, cols] row-major, tiles of 64 columns x box_rows rows, 128B swizzle,
+// rows past the end read as zero.
+dflash_status make_tmap(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t cols, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(dfl::kLmTileK), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(DFLASH_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a [%lld, %lld] tensor", static_cast<int>(r),
+                    static_cast<long long>(rows), static_cast<long long>(cols));
+    return ok();
+}
+
+constexpr size_t kSmemLimit = 232448;  // opt-in shared memory per block on sm_100-class GPUs
+constexpr int kProfileRuns = 4096;
+constexpr int kProfileKernels = 4;
+
+struct Plan {
+    int N, NT, n_tiles_n, G, grid, stages, R_total, ksplit;
+    size_t smem;
+};
+
+}  // namespace
+
+struct dflash_select_ctx {
+    dflash_select_config cfg;
+    const void *W, *E, *WA, *WB, *WH;
+    int device = 0, num_sms = 0;
+    CUtensorMap tm_w, tm_gate, tm_h;
+    const void *h_ptr = nullptr;
+    int h_rows = -1;
+    int m_tiles_vocab = 0, m_tiles_total = 0, R = 0;
+
+    void *ws = nullptr;
+    uint64_t *part = nullptr;
+    float *gate = nullptr, *vals = nullptr, *AB = nullptr, *P = nullptr;
+    int32_t *ids = nullptr;
+    unsigned *ticket = nullptr;
+    int *err = nullptr;
+    // staging of dflash_select_step_host
+    uint16_t *st_hidden = nullptr;
+    int32_t *st_anchor = nullptr, *st_target = nullptr, *st_path = nullptr, *st_accept = nullptr,
+            *st_emitted = nullptr;
+    int *err_host = nullptr;  // pinned
+
+    bool prof = false;
+    int prof_runs = 0;
+    std::vector<cudaEvent_t> ev;  // kProfileRuns x (kProfileKernels + 1)
+
+    Plan plan(int B) const
+    {
+        Plan p;
+        p.N = B * cfg.L;
+        p.NT = p.N <= 256 ? ((p.N + 15) / 16) * 16 : 256;
+        p.n_tiles_n = (p.N + p.NT - 1) / p.NT;
+        int g = num_sms / p.n_tiles_n;
+        if (g < 1) g = 1;
+        if (g > m_tiles_total) g = m_tiles_total;
+        p.G = g;
+        p.grid = g * p.n_tiles_n;
+        const size_t fixed = dfl::lmhead_smem_bytes(p.NT, cfg.K, 0);
+        const size_t stage = static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 +
+                             static_cast<size_t>(p.NT) * dfl::kLmTileK * 2;
+        int st = static_cast<int>((kSmemLimit - fixed) / stage);
+        if (st > dfl::kLmMaxStages) st = dfl::kLmMaxStages;
+        p.stages = st;
+        p.smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, st);
+        p.R_total = B * R;
+        p.ksplit = dfl::projection_ksplit(cfg.d, p.R_total, num_sms);
+        return p;
+    }
+};
+
+extern "C" {
+
+const char *dflash_last_error(void)
+{
+    return g_last_error.c_str();
+}
+
+static dflash_status check_config(const dflash_select_config *c)
+{
+    if (!c) return fail(DFLASH_ERR_INVALID_ARG, "config is NULL");
+    if (c->K != 16 && c->K != 32) return fail(DFLASH_ERR_UNSUPPORTED, "K must be 16 or 32 (got %d)", c->K);
+    if (c->L < 1 || c->L > 16) return fail(DFLASH_ERR_UNSUPPORTED, "L must be in [1, 16] (got %d)", c->L);
+    if (c->V < c->K || c->V >= (int64_t(1) << 31))
+        return fail(DFLASH_ERR_UNSUPPORTED, "V must satisfy K <= V < 2^31 (got %lld)", static_cast<long long>(c->V));
+    if (c->d < 64 || c->d > 16384 || c->d % 64 != 0)
+        return fail(DFLASH_ERR_UNSUPPORTED, "d must be a multiple of 64 in [64, 16384] (got %d)", c->d);
+    if (c->e != dfl::kEmbed) return fail(DFLASH_ERR_UNSUPPORTED, "e must be 256 (got %d)", c->e);
+    if (c->max_batch < 1 || static_cast<int64_t>(c->max_batch) * c->L > 8192)
+        return fail(DFLASH_ERR_UNSUPPORTED, "max_batch must be >= 1 with max_batch * L <= 8192");
+    if (c->walk != DFLASH_WALK_VITERBI && c->walk != DFLASH_WALK_GREEDY)
+        return fail(DFLASH_ERR_INVALID_ARG, "walk must be DFLASH_WALK_VITERBI or DFLASH_WALK_GREEDY");
+    if (!(c->tie_eps >= 0.0f) || !std::isfinite(c->tie_eps))
+        return fail(DFLASH_ERR_INVALID_ARG, "tie_eps must be finite and >= 0");
+    return ok();
+}
+
+dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_lm, const void *E, const void *W_A,
+                                 const void *W_B, const void *W_H, void *stream, dflash_select_handle *out)
+{
+    if (!out) return fail(DFLASH_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    dflash_status st = check_config(cfg);
+    if (st != DFLASH_OK) return st;
+    const void *ptrs[5] = {W_lm, E, W_A, W_B, W_H};
+    const char *names[5] = {"W_lm", "E", "W_A", "W_B", "W_H"};
+    for (int i = 0; i < 5; ++i) {
+        if (!ptrs[i]) return fail(DFLASH_ERR_INVALID_ARG, "%s is NULL", names[i]);
+        if (!aligned16(ptrs[i])) return fail(DFLASH_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+    }
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    cudaDeviceProp prop;
+    CUDA_TRY(cudaGetDeviceProperties(&prop, dev));
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(DFLASH_ERR_UNSUPPORTED, "this library is built for sm_103 (GB300); device is sm_%d%d", prop.major,
+                    prop.minor);
+
+    dflash_select_ctx *c = new (std::nothrow) dflash_select_ctx();
+    if (!c) return fail(DFLASH_ERR_CUDA, "out of host memory");
+    c->cfg = *cfg;
+    c->W = W_lm;
+    c->E = E;
+    c->WA = W_A;
+    c->WB = W_B;
+    c->WH = W_H;
+    c->device = dev;
+    c->num_sms = prop.multiProcessorCount;
+    c->m_tiles_vocab = static_cast<int>((cfg->V + dfl::kLmTileM - 1) / dfl::kLmTileM);
+    c->m_tiles_total = c->m_tiles_vocab + dfl::kEmbed / dfl::kLmTileM;
+    c->R = cfg->L * cfg->K + 1;
+
+    if ((st = make_tmap(&c->tm_w, W_lm, cfg->V, cfg->d, dfl::kLmTileM)) != DFLASH_OK ||
+        (st = make_tmap(&c->tm_gate, W_H, dfl::kEmbed, cfg->d, dfl::kLmTileM)) != DFLASH_OK) {
+        delete c;
+        return st;
+    }
+
+    // workspace: the largest partial-list buffer over every batch size
+    size_t part_elems = 0;
+    for (int B = 1; B <= cfg->max_batch; ++B) {
+        Plan p = c->plan(B);
+        size_t e = static_cast<size_t>(p.G) * p.N * cfg->K;
+        if (e > part_elems) part_elems = e;
+    }
+    const size_t Nmax = static_cast<size_t>(cfg->max_batch) * cfg->L;
+    const size_t Bm = static_cast<size_t>(cfg->max_batch);
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    size_t off = 0;
+    const size_t o_part = off; off += up(part_elems * 8);
+    const size_t o_gate = off; off += up(Nmax * dfl::kEmbed * 4);
+    const size_t o_ids = off; off += up(Nmax * cfg->K * 4);
+    const size_t o_vals = off; off += up(Nmax * cfg->K * 4);
+    const size_t o_AB = off; off += up(Bm * c->R * 512 * 4);
+    const size_t o_P = off; off += up(Nmax * cfg->K * cfg->K * 4);
+    const size_t o_ticket = off; off += up(Bm * 4);
+    const size_t o_err = off; off += up(4);
+    const size_t o_hid = off; off += up(Nmax * cfg->d * 2);
+    const size_t o_anc = off; off += up(Bm * 4);
+    const size_t o_tgt = off; off += up(Bm * (cfg->L + 1) * 4);
+    const size_t o_path = off; off += up(Nmax * 4);
+    const size_t o_acc = off; off += up(Bm * 4);
+    const size_t o_emit = off; off += up(Bm * (cfg->L + 1) * 4);
+    cudaError_t e = cudaMalloc(&c->ws, off);
+    if (e != cudaSuccess) {
+        delete c;
+        return fail(DFLASH_ERR_CUDA, "cudaMalloc of a %zu-byte workspace failed: %s", off, cudaGetErrorString(e));
+    }
+    e = cudaMallocHost(&c->err_host, sizeof(int));
+    if (e != cudaSuccess) {
+        cudaFree(c->ws);
+        delete c;
+        return fail(DFLASH_ERR_CUDA, "cudaMallocHost failed: %s", cudaGetErrorString(e));
+    }
+    uint8_t *w = static_cast<uint8_t *>(c->ws);
+    c->part = reinterpret_cast<uint64_t *>(w + o_part);
+    c->gate = reinterpret_cast<float *>(w + o_gate);
+    c->ids = reinterpret_cast<int32_t *>(w + o_ids);
+    c->vals = reinterpret_cast<float *>(w + o_vals);
+    c->AB = reinterpret_cast<float *>(w + o_AB);
+    c->P = reinterpret_cast<float *>(w + o_P);
+    c->ticket = reinterpret_cast<unsigned *>(w + o_ticket);
+    c->err = reinterpret_cast<int *>(w + o_err);
+    c->st_hidden = reinterpret_cast<uint16_t *>(w + o_hid);
+    c->st_anchor = reinterpret_cast<int32_t *>(w + o_anc);
+    c->st_target = reinterpret_cast<int32_t *>(w + o_tgt);
+    c->st_path = reinterpret_cast<int32_t *>(w + o_path);
+    c->st_accept = reinterpret_cast<int32_t *>(w + o_acc);
+    c->st_emitted = reinterpret_cast<int32_t *>(w + o_emit);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(c->ws, 0, off, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        cudaFreeHost(c->err_host);
+        cudaFree(c->ws);
+        delete c;
+        return fail(DFLASH_ERR_CUDA, "workspace initialisation failed: %s", cudaGetErrorString(e));
+    }
+    *out = c;
+    return ok();
+}
+
+static void prof_ensure(dflash_select_ctx *c)
+{
+    if (!c->ev.empty()) return;
+    c->ev.resize(static_cast<size_t>(kProfileRuns) * (kProfileKernels + 1));
+    for (auto &x : c->ev) cudaEventCreate(&x);
+}
+
+static void prof_mark(dflash_select_ctx *c, int k, cudaStream_t s)
+{
+    if (c->prof && c->prof_runs < kProfileRuns)
+        cudaEventRecord(c->ev[static_cast<size_t>(c->prof_runs) * (kProfileKernels + 1) + k], s);
+}
+
+dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,
+                                int32_t *topk_ids, float *topk_vals, float *pair_scores, int32_t *path,
+                                float *path_score, uint8_t *tie_flags, void *stream)
+{
+    if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+    dflash_select_ctx *c = h;
+    if (B < 0 || B > c->cfg.max_batch)
+        return fail(DFLASH_ERR_INVALID_ARG, "B must be in [0, max_batch=%d] (got %d)", c->cfg.max_batch, B);
+    if (B == 0) return ok();
+    if (!hidden || !anchor || !path) return fail(DFLASH_ERR_INVALID_ARG, "hidden, anchor and path must not be NULL");
+    if (!aligned16(hidden)) return fail(DFLASH_ERR_INVALID_ARG, "hidden is not 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Plan pl = c->plan(B);
+    if (hidden != c->h_ptr || pl.N != c->h_rows) {
+        dflash_status st = make_tmap(&c->tm_h, hidden, pl.N, c->cfg.d, pl.NT);
+        if (st != DFLASH_OK) return st;
+        c->h_ptr = hidden;
+        c->h_rows = pl.N;
+    }
+
+    dfl::LmHeadParams lp;
+    lp.tm_w = c->tm_w;
+    lp.tm_gate = c->tm_gate;
+    lp.tm_h = c->tm_h;
+    lp.V = c->cfg.V;
+    lp.d = c->cfg.d;
+    lp.N = pl.N;
+    lp.NT = pl.NT;
+    lp.n_tiles_n = pl.n_tiles_n;
+    lp.K = c->cfg.K;
+    lp.m_tiles_vocab = c->m_tiles_vocab;
+    lp.m_tiles_total = c->m_tiles_total;
+    lp.ctas_per_ntile = pl.G;
+    lp.stages = pl.stages;
+    lp.part = c->part;
+    lp.gate = c->gate;
+    lp.err = c->err;
+
+    prof_mark(c, 0, s);
+    CUDA_TRY(dfl::launch_lmhead_topk(lp, pl.grid, pl.smem, s));
+    prof_mark(c, 1, s);
+    CUDA_TRY(dfl::launch_topk_merge(c->part, pl.G, pl.N, c->cfg.K, c->ids, c->vals, topk_ids, topk_vals, s));
+    prof_mark(c, 2, s);
+
+    dfl::ProjParams pp;
+    pp.E = static_cast<const uint16_t *>(c->E);
+    pp.WA = static_cast<const uint16_t *>(c->WA);
+    pp.WB = static_cast<const uint16_t *>(c->WB);
+    pp.ids = c->ids;
+    pp.anchor = anchor;
+    pp.AB = c->AB;
+    pp.err = c->err;
+    pp.V = c->cfg.V;
+    pp.d = c->cfg.d;
+    pp.L = c->cfg.L;
+    pp.K = c->cfg.K;
+    pp.R = c->R;
+    pp.R_total = pl.R_total;
+    pp.ksplit = pl.ksplit;
+    pp.kchunk = c->cfg.d / pl.ksplit;
+    CUDA_TRY(dfl::launch_projection(pp, s));
+    prof_mark(c, 3, s);
+
+    dfl::PairParams q;
+    q.AB = c->AB;
+    q.gate = c->gate;
+    q.vals = c->vals;
+    q.ids = c->ids;
+    q.P = c->P;
+    q.P_out = pair_scores;
+    q.ticket = c->ticket;
+    q.path = path;
+    q.path_score = path_score;
+    q.tie_flags = tie_flags;
+    q.B = B;
+    q.L = c->cfg.L;
+    q.K = c->cfg.K;
+    q.R = c->R;
+    q.walk = c->cfg.walk;
+    q.tie_eps = c->cfg.tie_eps;
+    CUDA_TRY(dfl::launch_pair_walk(q, s));
+    prof_mark(c, 4, s);
+    if (c->prof && c->prof_runs < kProfileRuns) ++c->prof_runs;
+    return ok();
+}
+
+dflash_status dflash_verify_prefix(const int32_t *path, const int32_t *target, int32_t B, int32_t L,
+                                   int32_t *accept_len, int32_t *emitted, void *stream)
+{
+    if (B < 0) return fail(DFLASH_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
+    if (L < 1 || L > 16) return fail(DFLASH_ERR_INVALID_ARG, "L must be in [1, 16] (got %d)", L);
+    if (B == 0) return ok();
+    if (!path || !target || !accept_len)
+        return fail(DFLASH_ERR_INVALID_ARG, "path, target and accept_len must not be NULL");
+    CUDA_TRY(dfl::launch_verify(path, target, B, L, accept_len, emitted, static_cast<cudaStream_t>(stream)));
+    return ok();
+}
+
+static dflash_status read_device_error(dflash_select_ctx *c, cudaStream_t s)
+{
+    CUDA_TRY(cudaMemcpyAsync(c->err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    const int e = *c->err_host;
+    if (e == 0) return ok();
+    CUDA_TRY(cudaMemsetAsync(c->err, 0, sizeof(int), s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    if (e & dfl::DEV_ERR_TIMEOUT)
+        return fail(DFLASH_ERR_TIMEOUT, "a kernel pipeline wait exceeded its time bound (device error word %d)", e);
+    return fail(DFLASH_ERR_DEVICE_CHECK, "a token id outside [0, V) reached the selector (device error word %d)", e);
+}
+
+dflash_status dflash_select_step_host(dflash_select_handle h, const void *hidden_host, const int32_t *anchor_host,
+                                      const int32_t *target_host, int32_t B, int32_t *path_host, int32_t *accept_host,
+                                      int32_t *emitted_host, void *stream)
+{
+    if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+    dflash_select_ctx *c = h;
+    if (B < 0 || B > c->cfg.max_batch)
+        return fail(DFLASH_ERR_INVALID_ARG, "B must be in [0, max_batch=%d] (got %d)", c->cfg.max_batch, B);
+    if (B == 0) return ok();
+    if (!hidden_host || !anchor_host || !target_host || !path_host || !accept_host || !emitted_host)
+        return fail(DFLASH_ERR_INVALID_ARG, "host buffers must not be NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int L = c->cfg.L;
+    const size_t nb = static_cast<size_t>(B);
+    CUDA_TRY(cudaMemcpyAsync(c->st_hidden, hidden_host, nb * L * c->cfg.d * 2, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(c->st_anchor, anchor_host, nb * 4, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(c->st_target, target_host, nb * (L + 1) * 4, cudaMemcpyHostToDevice, s));
+    dflash_status st = dflash_select_run(h, c->st_hidden, c->st_anchor, B, nullptr, nullptr, nullptr, c->st_path,
+                                         nullptr, nullptr, stream);
+    if (st != DFLASH_OK) return st;
+    st = dflash_verify_prefix(c->st_path, c->st_target, B, L, c->st_accept, c->st_emitted, stream);
+    if (st != DFLASH_OK) return st;
+    CUDA_TRY(cudaMemcpyAsync(path_host, c->st_path, nb * L * 4, cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaMemcpyAsync(accept_host, c->st_accept, nb * 4, cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaMemcpyAsync(emitted_host, c->st_emitted, nb * (L + 1) * 4, cudaMemcpyDeviceToHost, s));
+    return read_device_error(c, s);
+}
+
+dflash_status dflash_select_sync_status(dflash_select_handle h, void *stream)
+{
+    if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+    return read_device_error(h, static_cast<cudaStream_t>(stream));
+}
+
+dflash_status dflash_select_profile(dflash_select_handle h, int32_t enable)
+{
+    if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+    if (enable) prof_ensure(h);
+    h->prof = enable != 0;
+    if (enable) h->prof_runs = 0;
+    return ok();
+}
+
+dflash_status dflash_select_profile_read(dflash_select_handle h, double *ms_total, int64_t *launches,
+                                         int32_t max_kernels, int32_t *n_kernels)
+{
+    if (!h || !ms_total || !launches || !n_kernels) return fail(DFLASH_ERR_INVALID_ARG, "NULL argument");
+    const int nk = max_kernels < kProfileKernels ? max_kernels : kProfileKernels;
+    for (int k = 0; k < nk; ++k) {
+        ms_total[k] = 0.0;
+        launches[k] = 0;
+    }
+    for (int r = 0; r < h->prof_runs; ++r) {
+        cudaEvent_t *e = &h->ev[static_cast<size_t>(r) * (kProfileKernels + 1)];
+        CUDA_TRY(cudaEventSynchronize(e[kProfileKernels]));
+        for (int k = 0; k < nk; ++k) {
+            float ms = 0.f;
+            CUDA_TRY(cudaEventElapsedTime(&ms, e[k], e[k + 1]));
+            ms_total[k] += ms;
+            launches[k] += 1;
+        }
+    }
+    *n_kernels = nk;
+    return ok();
+}
+
+int32_t dflash_select_launches_per_run(dflash_select_handle h, int32_t B)
+{
+    (void)h;
+    return B > 0 ? 4 : 0;
+}
+
+dflash_status dflash_select_destroy(dflash_select_handle h)
+{
+    if (!h) return ok();
+    dflash_status st = DFLASH_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        st = fail(DFLASH_ERR_CUDA, "device synchronisation failed before destroy");
+    } else {
+        int e = 0;
+        if (cudaMemcpy(&e, h->err, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess && e != 0)
+            st = (e & dfl::DEV_ERR_TIMEOUT) ? fail(DFLASH_ERR_TIMEOUT, "pending device timeout at destroy")
+                                            : fail(DFLASH_ERR_DEVICE_CHECK, "pending out-of-range token at destroy");
+    }
+    for (auto &x : h->ev) cudaEventDestroy(x);
+    cudaFreeHost(h->err_host);
+    cudaFree(h->ws);
+    delete h;
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// Launch interfaces of the path-selector kernels (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dfl {
+
+// Bits of the device error word.
+enum : int { DEV_ERR_TOKEN = 1, DEV_ERR_TIMEOUT = 2 };
+
+constexpr int kEmbed = 256;  // width of A, B and the context gate
+
+// ---- lm_head GEMM + streaming top-K (and the context gate g = W_H h) ----
+constexpr int kLmTileM = 128;   // vocabulary rows per MMA tile (TMEM lanes)
+constexpr int kLmTileK = 64;    // hidden columns per pipeline stage (128 B rows)
+constexpr int kLmThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kLmMaxStages = 8;
+
+struct LmHeadParams {
+    CUtensorMap tm_w;     // lm_head W [V, d] bf16, box 64 x 128, 128B swizzle
+    CUtensorMap tm_gate;  // W_H [256, d] bf16, box 64 x 128
+    CUtensorMap tm_h;     // hidden [N, d] bf16, box 64 x NT
+    int64_t V;
+    int d, N, NT, n_tiles_n, K;
+    int m_tiles_vocab, m_tiles_total, ctas_per_ntile, stages;
+    uint64_t *part;  // [ctas_per_ntile][N][K] partial top-K keys
+    float *gate;     // [N][256] g_t = W_H h_t
+    int *err;
+};
+
+size_t lmhead_smem_bytes(int NT, int K, int stages);
+cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s);
+
+// Merges the partial lists of every CTA into the sorted top-K of each position.
+cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws,
+                              float *vals_ws, int32_t *ids_out, float *vals_out, cudaStream_t s);
+
+// ---- candidate projections A|B = [W_A; W_B] E[row] (mma.sync, cluster split-K) ----
+struct ProjParams {
+    const uint16_t *E, *WA, *WB;  // bf16 bits
+    const int32_t *ids;           // [B, L, K] merged candidates
+    const int32_t *anchor;        // [B]
+    float *AB;                    // [B * R][512]: cols 0..255 = A, 256..511 = B
+    int *err;
+    int64_t V;
+    int d, L, K, R, R_total, ksplit, kchunk;
+};
+cudaError_t launch_projection(const ProjParams &p, cudaStream_t s);
+int projection_ksplit(int d, int R_total, int num_sms);
+
+// ---- pair tables and the walk ----
+struct PairParams {
+    const float *AB;      // [B * R][512]
+    const float *gate;    // [B * L][256]
+    const float *vals;    // [B, L, K]
+    const int32_t *ids;   // [B, L, K]
+    float *P;             // [B, L, K, K] workspace tables
+    float *P_out;         // optional copy for the caller
+    unsigned *ticket;     // [B] zero between runs
+    int32_t *path;        // [B, L]
+    float *path_score;    // optional [B]
+    uint8_t *tie_flags;   // optional [B, L]
+    int B, L, K, R, walk;
+    float tie_eps;
+};
+cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s);
+
+// ---- greedy accept check ----
+cudaError_t launch_verify(const int32_t *path, const int32_t *target, int B, int L, int32_t *accept,
+                          int32_t *emitted, cudaStream_t s);
+
+}  // namespace dfl

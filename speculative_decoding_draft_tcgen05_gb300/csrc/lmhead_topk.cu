@@ -1,0 +1,350 @@
+// Fused lm_head GEMM + streaming top-K for the DFlash 2 path selector.
+//
+// Blog "DFlash 2: Keep Drafting Parallel", section "A Lightweight Path
+// Selector": the selector keeps the drafter's 16 best candidates per draft
+// position, ranked by the drafter's own logit U_t(b) = W[b] . h_t, and gates
+// the pair score with H(h_t). Both are products of a [rows, d] weight with the
+// hidden states, so one kernel computes them from the same weight stream:
+//   - vocabulary tiles (128 rows of W) feed a running top-K per position;
+//   - two extra tiles (the 256 rows of W_H) write the gate g_t = W_H h_t.
+// The full logits never reach global memory.
+//
+// Swap-AB tcgen05 GEMM: the 128 weight rows of a tile are the MMA's M (TMEM
+// lanes), the NT positions of an n-tile are N (TMEM columns), K = d is
+// streamed 64 columns per stage by TMA into 128-byte-swizzled shared memory.
+// Warp roles per CTA (persistent, one CTA per SM):
+//   warp 0      TMA producer (one thread), `stages`-deep ring
+//   warp 1      TMEM owner and MMA issuer (one thread), two accumulators
+//   warps 2..5  epilogue: TMEM -> registers -> transpose through shared
+//               memory -> per-position threshold filter -> warp-sorted insert
+// Each CTA owns one n-tile and every ctas_per_ntile-th M tile; it writes one
+// sorted partial list of K keys per position, merged by topk_merge_kernel.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dfl {
+
+namespace {
+
+constexpr uint32_t kTileABytes = kLmTileM * kLmTileK * 2;  // 16 KB
+constexpr uint32_t kTransposeBytes = 16 * kLmTileM * 4;    // 16 columns x 128 rows fp32
+
+__device__ __forceinline__ void named_bar_sync(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Barrier over the epilogue warps that also ORs a predicate across them, so
+// that every epilogue thread takes the same abort decision.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+__host__ __device__ inline uint32_t tmem_cols_for(int NT)
+{
+    uint32_t need = 2u * static_cast<uint32_t>(NT), c = 32;
+    while (c < need) c <<= 1;
+    return c;
+}
+
+struct Layout {
+    uint32_t stage_bytes, off_T, off_list, off_thr, off_bar, total;
+};
+
+__host__ __device__ inline Layout make_layout(int NT, int K, int stages)
+{
+    Layout l;
+    l.stage_bytes = kTileABytes + static_cast<uint32_t>(NT) * kLmTileK * 2;
+    l.off_T = stages * l.stage_bytes;
+    l.off_list = l.off_T + kTransposeBytes;
+    l.off_thr = l.off_list + static_cast<uint32_t>(NT) * K * 8;
+    l.off_bar = l.off_thr + static_cast<uint32_t>(NT) * 8;
+    // full[S], empty[S], tfull[2], tempty[2], drain, then tmem base + abort flag
+    l.total = l.off_bar + 8u * (2u * stages + 5u) + 16u;
+    return l;
+}
+
+__global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid_constant__ LmHeadParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 128B-swizzled tiles need 1024 B alignment
+    uint8_t *const gbase = smem_raw + (base - raw);
+
+    const int NT = p.NT, K = p.K, S = p.stages;
+    const Layout lay = make_layout(NT, K, S);
+    float *const T = reinterpret_cast<float *>(gbase + lay.off_T);
+    uint64_t *const lists = reinterpret_cast<uint64_t *>(gbase + lay.off_list);
+    uint64_t *const thr = reinterpret_cast<uint64_t *>(gbase + lay.off_thr);
+    const uint32_t bar_full = base + lay.off_bar;
+    const uint32_t bar_empty = bar_full + 8u * S;
+    const uint32_t bar_tfull = bar_empty + 8u * S;
+    const uint32_t bar_tempty = bar_tfull + 16u;
+    const uint32_t bar_drain = bar_tempty + 16u;
+    uint32_t *const tmem_holder = reinterpret_cast<uint32_t *>(gbase + lay.off_bar + 8u * (2u * S + 5u));
+    volatile int *const abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tile = blockIdx.x % p.n_tiles_n;
+    const int chunk = blockIdx.x / p.n_tiles_n;
+    const int G = p.ctas_per_ntile;
+    const int KB = p.d / kLmTileK;
+    const uint32_t tmem_cols = tmem_cols_for(NT);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_full + 8u * s, 1);
+            mbar_init(bar_empty + 8u * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_tfull + 8u * a, 1);
+            mbar_init(bar_tempty + 8u * a, 128);
+        }
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < NT * K; i += kLmThreads) lists[i] = 0;
+    for (int i = threadIdx.x; i < NT; i += kLmThreads) thr[i] = 0;
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.tm_w);
+        tma_prefetch_desc(&p.tm_gate);
+        tma_prefetch_desc(&p.tm_h);
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc(smem_u32(tmem_holder), tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+            const uint64_t pol_h = l2_policy_evict_last();   // hidden: re-read by every CTA
+            int it = 0;
+            bool ok = true;
+            for (int m = chunk; ok && m < p.m_tiles_total; m += G) {
+                const bool gate = m >= p.m_tiles_vocab;
+                const CUtensorMap *tma = gate ? &p.tm_gate : &p.tm_w;
+                const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
+                    if (!mbar_wait(bar_empty + 8u * s, ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + s * lay.stage_bytes;
+                    mbar_arrive_expect_tx(bar_full + 8u * s, lay.stage_bytes);
+                    tma_load_2d(sa, tma, kb * kLmTileK, row0, bar_full + 8u * s, pol_w);
+                    tma_load_2d(sa + kTileABytes, &p.tm_h, kb * kLmTileK, n_tile * NT, bar_full + 8u * s,
+                                pol_h);
+                }
+            }
+            if (!ok) {
+                atomicOr(p.err, DEV_ERR_TIMEOUT);
+                // let the copies already issued land before the CTA can exit
+                for (int j = (it > S ? it - S : 0); j < it; ++j)
+                    mbar_wait(bar_full + 8u * (j % S), static_cast<uint32_t>(j / S) & 1u, abort_flag, false);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kLmTileM, NT);
+            int it = 0, j = 0;
+            bool ok = true;
+            for (int m = chunk; ok && m < p.m_tiles_total; m += G, ++j) {
+                const int a = j & 1;
+                const uint32_t u = static_cast<uint32_t>(j >> 1);
+                if (!mbar_wait(bar_tempty + 8u * a, (u & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * NT);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
+                    if (!mbar_wait(bar_full + 8u * s, ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = base + s * lay.stage_bytes;
+                    const uint32_t sb = sa + kTileABytes;
+#pragma unroll
+                    for (int k = 0; k < kLmTileK / 16; ++k)
+                        umma_bf16(d_tmem, smem_desc_sw128(sa + 32u * k), smem_desc_sw128(sb + 32u * k), idesc,
+                                  (kb | k) != 0);
+                    umma_commit(bar_empty + 8u * s);  // frees the stage once these MMAs have read it
+                }
+                if (ok) umma_commit(bar_tfull + 8u * a);
+            }
+            if (!ok) atomicOr(p.err, DEV_ERR_TIMEOUT);
+            // every MMA must be finished before TMEM is released
+            umma_commit(bar_drain);
+            mbar_wait(bar_drain, 0, abort_flag, false);
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int ew = warp - 2;           // 0..3: column share
+        const int q = warp & 3;            // TMEM lane quadrant this warp may read
+        const int row = q * 32 + lane;     // tile row owned by this thread
+        const int col_base = n_tile * NT;
+        const int nvalid = min(NT, p.N - col_base);
+        const int ncols16 = (nvalid + 15) & ~15;
+        int j = 0;
+        bool ok = true;
+        for (int m = chunk; m < p.m_tiles_total; m += G, ++j) {
+            const int a = j & 1;
+            const uint32_t u = static_cast<uint32_t>(j >> 1);
+            const bool got = mbar_wait(bar_tfull + 8u * a, u & 1u, abort_flag);
+            if (named_bar_or(1, 128, !got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * NT);
+            const bool gate = m >= p.m_tiles_vocab;
+            const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
+            for (int c0 = 0; c0 < ncols16; c0 += 16) {
+                float v[16];
+                __syncwarp();
+                tmem_load16(taddr + static_cast<uint32_t>(c0), v);
+                if (gate) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int pos = col_base + c0 + jj;
+                        if (c0 + jj < nvalid) p.gate[static_cast<size_t>(pos) * kEmbed + row0 + row] = v[jj];
+                    }
+                    continue;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) T[jj * kLmTileM + row] = v[jj];
+                named_bar_sync(1, 128);
+                for (int cc = ew; cc < 16; cc += 4) {
+                    const int col = c0 + cc;
+                    if (col >= nvalid) continue;  // uniform across the warp
+                    uint64_t th = thr[col];
+                    uint64_t mine = 0;
+                    bool loaded = false;
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const int r = qq * 32 + lane;
+                        const int64_t id = static_cast<int64_t>(row0) + r;
+                        const uint64_t key =
+                            (id < p.V) ? make_key(T[cc * kLmTileM + r], static_cast<uint32_t>(id)) : 0ull;
+                        unsigned surv = __ballot_sync(0xFFFFFFFFu, key > th);
+                        while (surv) {
+                            const int src = __ffs(surv) - 1;
+                            surv &= surv - 1;
+                            const uint64_t x = shfl_u64(key, src);
+                            if (!loaded) {
+                                mine = (lane < K) ? lists[col * K + lane] : 0ull;
+                                loaded = true;
+                            }
+                            if (x > th) {
+                                mine = list_insert(mine, x, lane, K);
+                                th = shfl_u64(mine, K - 1);
+                            }
+                        }
+                    }
+                    if (loaded) {
+                        if (lane < K) lists[col * K + lane] = mine;
+                        if (lane == 0) thr[col] = th;
+                    }
+                }
+                named_bar_sync(1, 128);
+            }
+            tc_fence_before_sync();
+            mbar_arrive(bar_tempty + 8u * a);
+        }
+        if (!ok) atomicOr(p.err, DEV_ERR_TIMEOUT);
+        named_bar_sync(1, 128);
+        const int t0 = threadIdx.x - 64;
+        for (int i = t0; i < nvalid * K; i += 128) {
+            const int col = i / K;
+            p.part[(static_cast<size_t>(chunk) * p.N + col_base + col) * K + (i % K)] = lists[i];
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, tmem_cols);
+    }
+}
+
+// One CTA per position: every warp folds a share of the partial lists into a
+// running sorted list, then warp 0 folds the warps' lists together.
+__global__ void __launch_bounds__(256) topk_merge_kernel(const uint64_t *__restrict__ part, int G, int N,
+                                                         int K, int32_t *ids_ws, float *vals_ws,
+                                                         int32_t *ids_out, float *vals_out)
+{
+    __shared__ uint64_t wl[8][32];
+    const int col = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t run = 0;
+#pragma unroll 4
+    for (int g = warp; g < G; g += 8) {
+        const uint64_t x = (lane < K) ? part[(static_cast<size_t>(g) * N + col) * K + lane] : 0ull;
+        run = list_merge(run, x, lane, K);
+    }
+    wl[warp][lane] = run;
+    __syncthreads();
+    if (warp == 0) {
+        uint64_t r = wl[0][lane];
+        for (int w = 1; w < 8; ++w) r = list_merge(r, wl[w][lane], lane, K);
+        if (lane < K) {
+            const int32_t id = key_id(r);
+            const float v = key_val(r);
+            const size_t o = static_cast<size_t>(col) * K + lane;
+            ids_ws[o] = id;
+            vals_ws[o] = v;
+            if (ids_out) ids_out[o] = id;
+            if (vals_out) vals_out[o] = v;
+        }
+    }
+}
+
+}  // namespace
+
+size_t lmhead_smem_bytes(int NT, int K, int stages)
+{
+    return static_cast<size_t>(make_layout(NT, K, stages).total) + 1024;  // + alignment slack
+}
+
+cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    lmhead_topk_kernel<<<grid, kLmThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws, float *vals_ws,
+                              int32_t *ids_out, float *vals_out, cudaStream_t s)
+{
+    topk_merge_kernel<<<N, 256, 0, s>>>(part, G, N, K, ids_ws, vals_ws, ids_out, vals_out);
+    return cudaGetLastError();
+}
+
+}  // namespace dfl

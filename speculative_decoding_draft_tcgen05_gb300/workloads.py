@@ -24,6 +24,7 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass, field
 
+import numpy as np
 import torch
 
 E_DIM = 256  # width of the A/B token embeddings and of the context gate
@@ -130,16 +131,19 @@ def make_inputs(wl: Workload) -> Inputs:
     return Inputs(wl, W, E, W_A, W_B, W_H, hidden, anchor, target_rand, n0, near)
 
 
-def _bf16_step(bits: int, up: bool) -> int:
-    """The bf16 bit pattern one representable step above (up) or below ``bits``."""
-    if bits & 0x7FFF == 0:
-        return 0x0001 if up else 0x8001
-    positive = (bits & 0x8000) == 0
-    return bits + 1 if positive == up else bits - 1
+def _bf16_values(bits: np.ndarray) -> np.ndarray:
+    """float64 values of bf16 bit patterns (uint16 array)."""
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def _bits_to_f(bits: int) -> float:
-    return float(torch.tensor([bits], dtype=torch.int32).to(torch.int16).view(torch.bfloat16)[0])
+def _bf16_step(bits: np.ndarray, up: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns one representable step above (up) or below each entry of ``bits``."""
+    b = bits.astype(np.int64)
+    zero = (b & 0x7FFF) == 0
+    positive = (b & 0x8000) == 0
+    step = np.where(positive == up, b + 1, b - 1)
+    step = np.where(zero, np.where(up, 0x0001, 0x8001), step)
+    return step.astype(np.uint16)
 
 
 def plant_near_ties(hidden32: torch.Tensor, W: torch.Tensor, frac: float, g: torch.Generator,
@@ -161,42 +165,39 @@ def plant_near_ties(hidden32: torch.Tensor, W: torch.Tensor, frac: float, g: tor
     nplant = int(round(frac * npos))
     order = torch.randperm(npos, generator=g)[:nplant].tolist()
     toks = torch.randint(0, V, (nplant, 2), generator=g, dtype=torch.int64).tolist()
-    h = hidden32.to(torch.float64).reshape(npos, d)
+    h = hidden32.to(torch.float64).reshape(npos, d).numpy()
     out = hidden32.to(torch.bfloat16).reshape(npos, d).clone()
+    out_bits = out.view(torch.int16).numpy().view(np.uint16)
     planted = []
     for p, (v1, v2) in zip(order, toks):
         if v1 == v2:
             v2 = (v1 + 1) % V
-        w1 = W[v1].to(torch.float64)
-        w2 = W[v2].to(torch.float64)
+        w1 = W[v1].to(torch.float64).numpy()
+        w2 = W[v2].to(torch.float64).numpy()
         D = w1 - w2
         S = w1 + w2
         u = S - (D @ S) / (D @ D) * D
-        u = u / u.norm()
+        u = u / np.linalg.norm(u)
         hp = h[p] - (D @ h[p]) / (D @ D) * D
         hp = hp - (u @ hp) * u + beta * u
-        hb = hp.to(torch.bfloat16)
-        bits = [int(x) & 0xFFFF for x in hb.view(torch.int16).tolist()]
-        vals = hb.to(torch.float64).tolist()
-        Dl = D.tolist()
-        cur = sum(a * b for a, b in zip(Dl, vals))
-        cand = torch.argsort(D.abs(), descending=True)[:64].tolist()
+        bits = torch.from_numpy(hp).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+        vals = _bf16_values(bits)
+        cur = float(D @ vals)
+        cand = np.argsort(-np.abs(D))[:64]
         for _ in range(256):
             if abs(cur) < gap:
                 break
-            best = None
-            for i in cand:
-                up = (cur * Dl[i]) < 0  # raising h_i lowers |cur| when D_i and cur differ in sign
-                nb = _bf16_step(bits[i], up)
-                nv = _bits_to_f(nb)
-                new = cur + Dl[i] * (nv - vals[i])
-                if abs(new) < abs(cur) and (best is None or abs(new) < best[0]):
-                    best = (abs(new), i, nb, nv, new)
-            if best is None:
+            up = (cur * D[cand]) < 0  # raising h_i lowers |cur| when D_i and cur differ in sign
+            nb = _bf16_step(bits[cand], up)
+            new = cur + D[cand] * (_bf16_values(nb) - vals[cand])
+            k = int(np.argmin(np.abs(new)))
+            if abs(new[k]) >= abs(cur):
                 break
-            _, i, nb, nv, new = best
-            bits[i], vals[i], cur = nb, nv, new
-        out[p] = torch.tensor(bits, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+            i = cand[k]
+            bits[i] = nb[k]
+            vals[i] = _bf16_values(nb[k:k + 1])[0]
+            cur = float(new[k])
+        out_bits[p] = bits
         planted.append((p // L, p % L, v1, v2))
     return out.reshape(B, L, d), planted
 
