@@ -262,9 +262,8 @@ def run_ours(args):
     stream.synchronize()
     target = wl.plant_targets(out["path"].cpu(), inp.target_rand, inp.n0, w.V).to(dev)
 
-    def step():
-        pkg.dflash_select_run(sel.h, hidden, anchor, stream=stream, **out)
-        pkg.dflash_verify_prefix(out["path"], target, accept, emitted, stream=stream)
+    step = pkg.bind_step(sel.h, hidden, anchor, target=target, accept_len=accept, emitted=emitted, stream=stream,
+                         **out)
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -279,7 +278,6 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    pkg.dflash_select_profile(sel.h, True)
     clocks.start()
     time.sleep(0.3)  # let the sampler attach before the timed region
     with torch.cuda.stream(stream):
@@ -291,6 +289,14 @@ def run_ours(args):
     clk = clocks.stop()
     torch.cuda.synchronize(dev)
     ms = ev0.elapsed_time(ev1)
+    pkg.dflash_select_sync_status(sel.h, stream=stream)
+    # second timed pass with CUDA events around every kernel of the run (they
+    # serialise the launches, so the headline number above is taken without them)
+    pkg.dflash_select_profile(sel.h, True)
+    with torch.cuda.stream(stream):
+        for _ in range(min(args.steps, 4096)):
+            step()
+    stream.synchronize()
     prof = pkg.dflash_select_profile_read(sel.h)
     pkg.dflash_select_profile(sel.h, False)
     pkg.dflash_select_sync_status(sel.h, stream=stream)

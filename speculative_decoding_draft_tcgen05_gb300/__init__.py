@@ -184,6 +184,40 @@ def dflash_select_launches_per_run(handle, B: int) -> int:
     return int(lib().dflash_select_launches_per_run(handle, B))
 
 
+def bind_step(handle, hidden, anchor, path, target=None, accept_len=None, emitted=None, stream=None, **outs):
+    """Marshals the arguments of dflash_select_run (and, with target given,
+    dflash_verify_prefix) once and returns a zero-argument callable that makes
+    the same call(s) again; for tight loops over fixed buffers."""
+    import torch
+    L_ = lib()
+    B = anchor.shape[0]
+    run_args = (handle, _ptr(hidden, torch.bfloat16, "hidden"), _ptr(anchor, torch.int32, "anchor"), B,
+                _ptr(outs.get("topk_ids"), torch.int32, "topk_ids"), _ptr(outs.get("topk_vals"), torch.float32,
+                                                                          "topk_vals"),
+                _ptr(outs.get("pair_scores"), torch.float32, "pair_scores"), _ptr(path, torch.int32, "path"),
+                _ptr(outs.get("path_score"), torch.float32, "path_score"),
+                _ptr(outs.get("tie_flags"), torch.uint8, "tie_flags"), _stream(stream))
+    run = L_.dflash_select_run
+    if target is None:
+        def step():
+            st = run(*run_args)
+            if st:
+                _check(st, "dflash_select_run")
+        return step
+    ver_args = (_ptr(path, torch.int32, "path"), _ptr(target, torch.int32, "target"), B, path.shape[1],
+                _ptr(accept_len, torch.int32, "accept_len"), _ptr(emitted, torch.int32, "emitted"), _stream(stream))
+    ver = L_.dflash_verify_prefix
+
+    def step():
+        st = run(*run_args)
+        if st:
+            _check(st, "dflash_select_run")
+        st = ver(*ver_args)
+        if st:
+            _check(st, "dflash_verify_prefix")
+    return step
+
+
 def dflash_select_destroy(handle):
     _check(lib().dflash_select_destroy(handle), "dflash_select_destroy")
 

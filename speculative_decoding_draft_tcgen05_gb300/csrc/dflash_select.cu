@@ -192,6 +192,9 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
         return fail(DFLASH_ERR_UNSUPPORTED, "this library is built for sm_103 (GB300); device is sm_%d%d", prop.major,
                     prop.minor);
 
+    CUDA_TRY(dfl::prepare_lmhead());
+    CUDA_TRY(dfl::prepare_pair_walk());
+
     dflash_select_ctx *c = new (std::nothrow) dflash_select_ctx();
     if (!c) return fail(DFLASH_ERR_CUDA, "out of host memory");
     c->cfg = *cfg;

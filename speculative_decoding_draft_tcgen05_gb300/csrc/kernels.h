@@ -5,12 +5,48 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace dfl {
 
 // Bits of the device error word.
 enum : int { DEV_ERR_TOKEN = 1, DEV_ERR_TIMEOUT = 2 };
 
 constexpr int kEmbed = 256;  // width of A, B and the context gate
+
+// Launches `kern` with programmatic dependent launch allowed (the kernel may be
+// scheduled while its predecessor on the stream finishes; every kernel here
+// waits with griddepcontrol.wait before touching data a predecessor wrote) and,
+// if cluster_z > 1, thread-block clusters of (1, 1, cluster_z).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, int cluster_z,
+                      Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_z > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 1;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = static_cast<unsigned>(cluster_z);
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Sets the shared-memory opt-ins of every kernel on the current device.
+cudaError_t prepare_lmhead();
+cudaError_t prepare_pair_walk();
 
 // ---- lm_head GEMM + streaming top-K (and the context gate g = W_H h) ----
 constexpr int kLmTileM = 128;   // vocabulary rows per MMA tile (TMEM lanes)

@@ -130,6 +130,10 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
+    // the set-up above overlaps the previous kernel; hidden states, the
+    // partial lists and the gate are touched only once it has finished
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -292,35 +296,50 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     }
 }
 
-// One CTA per position: every warp folds a share of the partial lists into a
-// running sorted list, then warp 0 folds the warps' lists together.
-__global__ void __launch_bounds__(256) topk_merge_kernel(const uint64_t *__restrict__ part, int G, int N,
-                                                         int K, int32_t *ids_ws, float *vals_ws,
-                                                         int32_t *ids_out, float *vals_out)
+// One CTA per position. The G partial lists of the position are staged in
+// shared memory with coalesced loads; each of the 16 warps folds a share of
+// them into a sorted list, then the warps' lists are folded pairwise in a
+// tree (4 rounds).
+constexpr int kMergeWarps = 16;
+
+__global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint64_t *__restrict__ part, int G,
+                                                                      int N, int K, int32_t *ids_ws,
+                                                                      float *vals_ws, int32_t *ids_out,
+                                                                      float *vals_out)
 {
-    __shared__ uint64_t wl[8][32];
+    extern __shared__ uint64_t mlists[];  // [G][K]
+    __shared__ uint64_t wl[kMergeWarps][32];
+    pdl_trigger();
+    pdl_wait();
     const int col = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < G * K; i += blockDim.x) {
+        const int g = i / K, k = i % K;
+        mlists[i] = part[(static_cast<size_t>(g) * N + col) * K + k];
+    }
+    __syncthreads();
     uint64_t run = 0;
-#pragma unroll 4
-    for (int g = warp; g < G; g += 8) {
-        const uint64_t x = (lane < K) ? part[(static_cast<size_t>(g) * N + col) * K + lane] : 0ull;
+    for (int g = warp; g < G; g += kMergeWarps) {
+        const uint64_t x = (lane < K) ? mlists[g * K + lane] : 0ull;
         run = list_merge(run, x, lane, K);
     }
     wl[warp][lane] = run;
     __syncthreads();
-    if (warp == 0) {
-        uint64_t r = wl[0][lane];
-        for (int w = 1; w < 8; ++w) r = list_merge(r, wl[w][lane], lane, K);
-        if (lane < K) {
-            const int32_t id = key_id(r);
-            const float v = key_val(r);
-            const size_t o = static_cast<size_t>(col) * K + lane;
-            ids_ws[o] = id;
-            vals_ws[o] = v;
-            if (ids_out) ids_out[o] = id;
-            if (vals_out) vals_out[o] = v;
+    for (int step = 1; step < kMergeWarps; step <<= 1) {
+        if ((warp & (2 * step - 1)) == 0) {
+            run = list_merge(run, wl[warp + step][lane], lane, K);
+            wl[warp][lane] = run;
         }
+        __syncthreads();
+    }
+    if (warp == 0 && lane < K) {
+        const int32_t id = key_id(run);
+        const float v = key_val(run);
+        const size_t o = static_cast<size_t>(col) * K + lane;
+        ids_ws[o] = id;
+        vals_ws[o] = v;
+        if (ids_out) ids_out[o] = id;
+        if (vals_out) vals_out[o] = v;
     }
 }
 
@@ -331,20 +350,24 @@ size_t lmhead_smem_bytes(int NT, int K, int stages)
     return static_cast<size_t>(make_layout(NT, K, stages).total) + 1024;  // + alignment slack
 }
 
+cudaError_t prepare_lmhead()
+{
+    cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+}
+
 cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s)
 {
-    cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    lmhead_topk_kernel<<<grid, kLmThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_ex(lmhead_topk_kernel, dim3(grid), dim3(kLmThreads), smem, s, 1, p);
 }
 
 cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws, float *vals_ws,
                               int32_t *ids_out, float *vals_out, cudaStream_t s)
 {
-    topk_merge_kernel<<<N, 256, 0, s>>>(part, G, N, K, ids_ws, vals_ws, ids_out, vals_out);
-    return cudaGetLastError();
+    const size_t smem = static_cast<size_t>(G) * K * sizeof(uint64_t);
+    return launch_ex(topk_merge_kernel, dim3(N), dim3(kMergeWarps * 32), smem, s, 1, part, G, N, K, ids_ws,
+                     vals_ws, ids_out, vals_out);
 }
 
 }  // namespace dfl

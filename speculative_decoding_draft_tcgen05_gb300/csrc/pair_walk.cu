@@ -88,6 +88,15 @@ __global__ void __launch_bounds__(kPThreads) projection_kernel(const ProjParams 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint16_t *W = (mt < 2 ? p.WA : p.WB) + static_cast<size_t>((mt & 1) * kPM) * p.d;
 
+    // The weight slice does not depend on earlier kernels: pull it towards L2
+    // while the candidates are still being produced.
+    pdl_trigger();
+    for (int i = tid; i < kPM * (p.kchunk / 64); i += kPThreads) {
+        const int r = i / (p.kchunk / 64), c = i % (p.kchunk / 64);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(W + static_cast<size_t>(r) * p.d + kz * p.kchunk + c * 64));
+    }
+    pdl_wait();
+
     for (int r = tid; r < kPN; r += kPThreads) {
         const int gr = n0 + r;
         int32_t t = -1;
@@ -226,6 +235,8 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
     __shared__ float mg[16 * 32];       // incoming margins [t][j]
     __shared__ int is_last;
 
+    pdl_trigger();
+    pdl_wait();
     const int K = p.K, L = p.L, R = p.R;
     const int b = blockIdx.x / L, t = blockIdx.x % L;
     const int tid = threadIdx.x;
@@ -275,11 +286,20 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
         }
     }
     __syncthreads();
-    if (!is_last || tid >= 32) return;
+    if (!is_last) return;
 
     // ---------------- walk (one warp; lane j = candidate rank j)
+    // The sequence's L tables (L * K * K floats <= 2 * 256 * K) replace the
+    // projection tiles in shared memory; the other CTAs' writes are read
+    // around L1.
+    float *const Pb = pw_smem;
+    {
+        const float *src = p.P + static_cast<size_t>(b) * L * K * K;
+        for (int i = tid; i < L * K * K; i += blockDim.x) Pb[i] = __ldcg(src + i);
+    }
+    __syncthreads();
+    if (tid >= 32) return;
     const int lane = tid;
-    const float *Pb = p.P + static_cast<size_t>(b) * L * K * K;
     const bool active = lane < K;
     int ranks[16];
     float score;
@@ -287,14 +307,14 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
     for (int s = 0; s < L; ++s) flags[s] = 0;
 
     if (p.walk == 0) {
-        float delta = active ? __ldcg(Pb + lane) : -INFINITY;
+        float delta = active ? Pb[lane] : -INFINITY;
         for (int s = 1; s < L; ++s) {
             float best = -INFINITY, second = -INFINITY;
             int bi = 0;
             const float *Ps = Pb + static_cast<size_t>(s) * K * K;
             for (int i = 0; i < K; ++i) {
                 const float di = __shfl_sync(0xFFFFFFFFu, delta, i);
-                const float v = active ? di + __ldcg(Ps + i * K + lane) : -INFINITY;
+                const float v = active ? di + Ps[i * K + lane] : -INFINITY;
                 if (v > best) {
                     second = best;
                     best = v;
@@ -337,7 +357,7 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
         int prev = 0;
         float total = 0.f;
         for (int s = 0; s < L; ++s) {
-            const float v = active ? __ldcg(Pb + (static_cast<size_t>(s) * K + prev) * K + lane) : -INFINITY;
+            const float v = active ? Pb[(s * K + prev) * K + lane] : -INFINITY;
             float bv = v;
             int bj = lane;
             for (int off = 16; off > 0; off >>= 1) {
@@ -382,34 +402,25 @@ int projection_ksplit(int d, int R_total, int num_sms)
     return ks;
 }
 
-cudaError_t launch_projection(const ProjParams &p, cudaStream_t s)
+cudaError_t prepare_pair_walk()
 {
     cudaError_t e = cudaFuncSetAttribute(projection_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kProjSmem));
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(4, (p.R_total + kPN - 1) / kPN, p.ksplit);
-    cfg.blockDim = dim3(kPThreads);
-    cfg.dynamicSmemBytes = kProjSmem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = p.ksplit;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, projection_kernel, p);
+    return cudaFuncSetAttribute(pair_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(2u * kEmbed * 32 * sizeof(float)));
+}
+
+cudaError_t launch_projection(const ProjParams &p, cudaStream_t s)
+{
+    return launch_ex(projection_kernel, dim3(4, (p.R_total + kPN - 1) / kPN, p.ksplit), dim3(kPThreads), kProjSmem, s,
+                     p.ksplit, p);
 }
 
 cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s)
 {
     const size_t smem = 2u * kEmbed * p.K * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(pair_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    pair_walk_kernel<<<p.B * p.L, 256, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_ex(pair_walk_kernel, dim3(p.B * p.L), dim3(256), smem, s, 1, p);
 }
 
 }  // namespace dfl

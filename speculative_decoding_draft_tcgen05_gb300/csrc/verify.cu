@@ -7,6 +7,7 @@
 // the target contributes one more token (its argmax after that prefix).
 // One warp per sequence: lane t compares position t, a ballot finds the first
 // mismatch.
+#include "common.cuh"
 #include "kernels.h"
 
 namespace dfl {
@@ -17,6 +18,8 @@ __global__ void __launch_bounds__(256) verify_kernel(const int32_t *__restrict__
                                                      const int32_t *__restrict__ target, int B, int L,
                                                      int32_t *__restrict__ accept, int32_t *__restrict__ emitted)
 {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (b >= B) return;
@@ -37,8 +40,8 @@ cudaError_t launch_verify(const int32_t *path, const int32_t *target, int B, int
                           int32_t *emitted, cudaStream_t s)
 {
     const int per_cta = 8;
-    verify_kernel<<<(B + per_cta - 1) / per_cta, per_cta * 32, 0, s>>>(path, target, B, L, accept, emitted);
-    return cudaGetLastError();
+    return launch_ex(verify_kernel, dim3((B + per_cta - 1) / per_cta), dim3(per_cta * 32), 0, s, 1, path, target, B,
+                     L, accept, emitted);
 }
 
 }  // namespace dfl
