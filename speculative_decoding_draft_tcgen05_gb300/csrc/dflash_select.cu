@@ -85,7 +85,6 @@ dflash_status make_tmap(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t 
     return ok();
 }
 
-constexpr size_t kSmemLimit = 232448;  // opt-in shared memory per block on sm_100-class GPUs
 constexpr int kProfileRuns = 4096;
 constexpr int kProfileKernels = 4;
 
@@ -100,6 +99,7 @@ struct dflash_select_ctx {
     dflash_select_config cfg;
     const void *W, *E, *WA, *WB, *WH;
     int device = 0, num_sms = 0;
+    size_t smem_optin = 0;  // opt-in shared memory per block
     CUtensorMap tm_w, tm_gate, tm_h;
     const void *h_ptr = nullptr;
     int h_rows = -1;
@@ -135,7 +135,7 @@ struct dflash_select_ctx {
         const size_t fixed = dfl::lmhead_smem_bytes(p.NT, cfg.K, 0);
         const size_t stage = static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 +
                              static_cast<size_t>(p.NT) * dfl::kLmTileK * 2;
-        int st = static_cast<int>((kSmemLimit - fixed) / stage);
+        int st = static_cast<int>((smem_optin - fixed) / stage);
         if (st > dfl::kLmMaxStages) st = dfl::kLmMaxStages;
         p.stages = st;
         p.smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, st);
@@ -192,8 +192,8 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
         return fail(DFLASH_ERR_UNSUPPORTED, "this library is built for sm_103 (GB300); device is sm_%d%d", prop.major,
                     prop.minor);
 
-    CUDA_TRY(dfl::prepare_lmhead());
-    CUDA_TRY(dfl::prepare_pair_walk());
+    CUDA_TRY(dfl::prepare_lmhead(static_cast<int>(prop.sharedMemPerBlockOptin)));
+    CUDA_TRY(dfl::prepare_pair_walk(static_cast<int>(prop.sharedMemPerBlockOptin)));
 
     dflash_select_ctx *c = new (std::nothrow) dflash_select_ctx();
     if (!c) return fail(DFLASH_ERR_CUDA, "out of host memory");
@@ -205,6 +205,7 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     c->WH = W_H;
     c->device = dev;
     c->num_sms = prop.multiProcessorCount;
+    c->smem_optin = prop.sharedMemPerBlockOptin;
     c->m_tiles_vocab = static_cast<int>((cfg->V + dfl::kLmTileM - 1) / dfl::kLmTileM);
     c->m_tiles_total = c->m_tiles_vocab + dfl::kEmbed / dfl::kLmTileM;
     c->R = cfg->L * cfg->K + 1;

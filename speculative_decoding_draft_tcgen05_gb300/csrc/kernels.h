@@ -44,9 +44,22 @@ cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Sets the shared-memory opt-ins of every kernel on the current device.
-cudaError_t prepare_lmhead();
-cudaError_t prepare_pair_walk();
+// Lets `kern` use as much dynamic shared memory as the device allows next to
+// its static shared memory.
+template <typename... KArgs>
+cudaError_t set_max_dynamic_smem(void (*kern)(KArgs...), int smem_optin)
+{
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_optin - static_cast<int>(fa.sharedSizeBytes));
+}
+
+// Sets the shared-memory opt-ins of every kernel on the current device
+// (smem_optin = cudaDevAttrMaxSharedMemoryPerBlockOptin).
+cudaError_t prepare_lmhead(int smem_optin);
+cudaError_t prepare_pair_walk(int smem_optin);
 
 // ---- lm_head GEMM + streaming top-K (and the context gate g = W_H h) ----
 constexpr int kLmTileM = 128;   // vocabulary rows per MMA tile (TMEM lanes)

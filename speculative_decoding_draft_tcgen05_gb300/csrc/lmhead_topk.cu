@@ -350,11 +350,11 @@ size_t lmhead_smem_bytes(int NT, int K, int stages)
     return static_cast<size_t>(make_layout(NT, K, stages).total) + 1024;  // + alignment slack
 }
 
-cudaError_t prepare_lmhead()
+cudaError_t prepare_lmhead(int smem_optin)
 {
-    cudaError_t e = cudaFuncSetAttribute(lmhead_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    cudaError_t e = set_max_dynamic_smem(lmhead_topk_kernel, smem_optin);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    return set_max_dynamic_smem(topk_merge_kernel, smem_optin);
 }
 
 cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s)

@@ -402,13 +402,11 @@ int projection_ksplit(int d, int R_total, int num_sms)
     return ks;
 }
 
-cudaError_t prepare_pair_walk()
+cudaError_t prepare_pair_walk(int smem_optin)
 {
-    cudaError_t e = cudaFuncSetAttribute(projection_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kProjSmem));
+    cudaError_t e = set_max_dynamic_smem(projection_kernel, smem_optin);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(pair_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(2u * kEmbed * 32 * sizeof(float)));
+    return set_max_dynamic_smem(pair_walk_kernel, smem_optin);
 }
 
 cudaError_t launch_projection(const ProjParams &p, cudaStream_t s)
