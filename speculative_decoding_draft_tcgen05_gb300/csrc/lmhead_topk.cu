@@ -130,35 +130,51 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
-    // the set-up above overlaps the previous kernel; hidden states, the
-    // partial lists and the gate are touched only once it has finished
+    // The set-up above overlaps the previous kernel on the stream. Hidden
+    // states, the partial lists and the gate are touched only after it has
+    // finished (griddepcontrol.wait); the constant weights may be read before.
     pdl_trigger();
-    pdl_wait();
+    if (!(warp == 0 && lane == 0)) pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
             const uint64_t pol_h = l2_policy_evict_last();   // hidden: re-read by every CTA
-            int it = 0;
+            const int n_my_tiles = (p.m_tiles_total - chunk + G - 1) / G;
+            const int total = n_my_tiles * KB;
+            // the first ring's weight tiles go out before the wait (the ring
+            // starts empty, so no slot has to be waited for)
+            const int pre = total < S ? total : S;
+            for (int it = 0; it < pre; ++it) {
+                const int m = chunk + (it / KB) * G, kb = it % KB;
+                const bool gate = m >= p.m_tiles_vocab;
+                const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
+                mbar_arrive_expect_tx(bar_full + 8u * it, lay.stage_bytes);
+                tma_load_2d(base + it * lay.stage_bytes, gate ? &p.tm_gate : &p.tm_w, kb * kLmTileK, row0,
+                            bar_full + 8u * it, pol_w);
+            }
+            pdl_wait();
+            for (int it = 0; it < pre; ++it)
+                tma_load_2d(base + it * lay.stage_bytes + kTileABytes, &p.tm_h, (it % KB) * kLmTileK, n_tile * NT,
+                            bar_full + 8u * it, pol_h);
+            int it = pre;
             bool ok = true;
-            for (int m = chunk; ok && m < p.m_tiles_total; m += G) {
+            for (; ok && it < total; ++it) {
+                const int m = chunk + (it / KB) * G, kb = it % KB;
                 const bool gate = m >= p.m_tiles_vocab;
                 const CUtensorMap *tma = gate ? &p.tm_gate : &p.tm_w;
                 const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
-                for (int kb = 0; kb < KB; ++kb, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
-                    if (!mbar_wait(bar_empty + 8u * s, ph ^ 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t sa = base + s * lay.stage_bytes;
-                    mbar_arrive_expect_tx(bar_full + 8u * s, lay.stage_bytes);
-                    tma_load_2d(sa, tma, kb * kLmTileK, row0, bar_full + 8u * s, pol_w);
-                    tma_load_2d(sa + kTileABytes, &p.tm_h, kb * kLmTileK, n_tile * NT, bar_full + 8u * s,
-                                pol_h);
+                const int s = it % S;
+                const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
+                if (!mbar_wait(bar_empty + 8u * s, ph ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
                 }
+                const uint32_t sa = base + s * lay.stage_bytes;
+                mbar_arrive_expect_tx(bar_full + 8u * s, lay.stage_bytes);
+                tma_load_2d(sa, tma, kb * kLmTileK, row0, bar_full + 8u * s, pol_w);
+                tma_load_2d(sa + kTileABytes, &p.tm_h, kb * kLmTileK, n_tile * NT, bar_full + 8u * s, pol_h);
             }
             if (!ok) {
                 atomicOr(p.err, DEV_ERR_TIMEOUT);
@@ -313,9 +329,21 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint
     pdl_wait();
     const int col = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < G * K; i += blockDim.x) {
-        const int g = i / K, k = i % K;
-        mlists[i] = part[(static_cast<size_t>(g) * N + col) * K + k];
+    // every load of a batch is issued before any of them is stored, so the
+    // batch costs one memory round trip
+    constexpr int kBatch = 10;
+    for (int i0 = 0; i0 < G * K; i0 += kBatch * kMergeWarps * 32) {
+        uint64_t v[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + u * kMergeWarps * 32 + threadIdx.x;
+            v[u] = (i < G * K) ? part[(static_cast<size_t>(i / K) * N + col) * K + (i % K)] : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + u * kMergeWarps * 32 + threadIdx.x;
+            if (i < G * K) mlists[i] = v[u];
+        }
     }
     __syncthreads();
     uint64_t run = 0;

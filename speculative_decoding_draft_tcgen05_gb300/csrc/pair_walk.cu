@@ -195,66 +195,88 @@ __global__ void __launch_bounds__(kPThreads) projection_kernel(const ProjParams 
     }
 
     const int ks = p.ksplit;
-    int r_begin = 0, r_end = kPN;
+    const float4 *const Ps4 = reinterpret_cast<const float4 *>(Ps);
+    constexpr int kRow4 = kPsStride / 4;  // float4 per staged row
     if (ks > 1) {
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();
         const int rank = static_cast<int>(cluster.block_rank());
-        r_begin = rank * (kPN / ks);
-        r_end = r_begin + kPN / ks;
-        for (int i = tid; i < (r_end - r_begin) * kPM; i += kPThreads) {
-            const int r = r_begin + i / kPM, o = i % kPM;
-            float s = 0.f;
-            for (int qq = 0; qq < ks; ++qq) {
-                const float *rem = cluster.map_shared_rank(Ps, qq);
-                s += rem[r * kPsStride + o];
-            }
+        const int rows = kPN / ks;
+        // rows [rank * rows, (rank + 1) * rows) of the tile, 128 outputs each,
+        // one float4 per thread per pass; the ks partial tiles are read from the
+        // peers' shared memory (all loads first, then the fixed-order sum)
+        for (int i = tid; i < rows * (kPM / 4); i += kPThreads) {
+            const int r = rank * rows + i / (kPM / 4), o4 = i % (kPM / 4);
+            float4 part[8];
+#pragma unroll
+            for (int qq = 0; qq < 8; ++qq)
+                if (qq < ks) part[qq] = cluster.map_shared_rank(Ps4, qq)[r * kRow4 + o4];
+            float4 sum = part[0];
+#pragma unroll
+            for (int qq = 1; qq < 8; ++qq)
+                if (qq < ks) {
+                    sum.x += part[qq].x;
+                    sum.y += part[qq].y;
+                    sum.z += part[qq].z;
+                    sum.w += part[qq].w;
+                }
             const int gr = n0 + r;
-            if (gr < p.R_total) p.AB[static_cast<size_t>(gr) * 512 + mt * kPM + o] = s;
+            if (gr < p.R_total)
+                *reinterpret_cast<float4 *>(p.AB + static_cast<size_t>(gr) * 512 + mt * kPM + o4 * 4) = sum;
         }
         cluster.sync();  // keep this CTA's tile alive until every peer has read it
     } else {
         __syncthreads();
-        for (int i = tid; i < kPN * kPM; i += kPThreads) {
-            const int r = i / kPM, o = i % kPM;
+        for (int i = tid; i < kPN * (kPM / 4); i += kPThreads) {
+            const int r = i / (kPM / 4), o4 = i % (kPM / 4);
             const int gr = n0 + r;
-            if (gr < p.R_total) p.AB[static_cast<size_t>(gr) * 512 + mt * kPM + o] = Ps[r * kPsStride + o];
+            if (gr < p.R_total)
+                *reinterpret_cast<float4 *>(p.AB + static_cast<size_t>(gr) * 512 + mt * kPM + o4 * 4) =
+                    Ps4[r * kRow4 + o4];
         }
     }
 }
 
 // grid B * L; block 256. Builds S_t for one (sequence, position); the last
-// CTA of a sequence to finish walks its tables.
+// CTA of a sequence to finish walks its tables. Every global load batch is
+// issued in full before its values are used (one round trip per batch).
+template <int K>
 __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
 {
     extern __shared__ float pw_smem[];
-    float *const Agt = pw_smem;                  // (A(prev_i) (.) g_t)[k] at [k * K + i]
-    float *const Bt = pw_smem + kEmbed * p.K;    // B(c_{t,j})[k] at [k * K + j]
-    __shared__ float vals[32];
-    __shared__ uint8_t bp[16 * 32];     // back-pointers [t][j]
-    __shared__ float mg[16 * 32];       // incoming margins [t][j]
+    float *const Agt = pw_smem;                // (A(prev_i) (.) g_t)[k] at [k * K + i]
+    float *const Bt = pw_smem + kEmbed * K;    // B(c_{t,j})[k] at [k * K + j]
+    __shared__ float vals[K];
+    __shared__ uint8_t bp[16 * K];             // back-pointers [t][j]
+    __shared__ float mg[16 * K];               // incoming margins [t][j]
+    __shared__ int ranks_s[16];
+    __shared__ uint8_t flags_s[16];
     __shared__ int is_last;
 
     pdl_trigger();
     pdl_wait();
-    const int K = p.K, L = p.L, R = p.R;
+    const int L = p.L, R = p.R;
     const int b = blockIdx.x / L, t = blockIdx.x % L;
     const int tid = threadIdx.x;
     const int n_prev = (t == 0) ? 1 : K;
     const size_t pos = static_cast<size_t>(b) * L + t;
 
     {
-        const int k = tid;  // blockDim.x == kEmbed
+        const int k = tid;  // blockDim.x == kEmbed: thread k owns component k
+        const size_t rowA0 = static_cast<size_t>(b) * R + (t == 0 ? 0 : 1 + (t - 1) * K);
+        const size_t rowB0 = static_cast<size_t>(b) * R + 1 + t * K;
+        float a[K], bb[K];
         const float gk = p.gate[pos * kEmbed + k];
-        for (int i = 0; i < n_prev; ++i) {
-            const size_t row = static_cast<size_t>(b) * R + (t == 0 ? 0 : 1 + (t - 1) * K + i);
-            Agt[k * K + i] = p.AB[row * 512 + k] * gk;
-        }
-        for (int j = 0; j < K; ++j) {
-            const size_t row = static_cast<size_t>(b) * R + 1 + t * K + j;
-            Bt[k * K + j] = p.AB[row * 512 + kEmbed + k];
-        }
-        if (tid < K) vals[tid] = p.vals[pos * K + tid];
+#pragma unroll
+        for (int i = 0; i < K; ++i) a[i] = (i < n_prev) ? p.AB[(rowA0 + i) * 512 + k] : 0.f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) bb[j] = p.AB[(rowB0 + j) * 512 + kEmbed + k];
+        const float v = (tid < K) ? p.vals[pos * K + tid] : 0.f;
+#pragma unroll
+        for (int i = 0; i < K; ++i) Agt[k * K + i] = a[i] * gk;
+#pragma unroll
+        for (int j = 0; j < K; ++j) Bt[k * K + j] = bb[j];
+        if (tid < K) vals[tid] = v;
     }
     __syncthreads();
 
@@ -264,10 +286,14 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
         const int i = e / K, jj = e % K;
         float s;
         if (i < n_prev) {
-            float dot = 0.f;
+            // two partial sums halve the dependent FMA chain
+            float d0 = 0.f, d1 = 0.f;
 #pragma unroll 8
-            for (int k = 0; k < kEmbed; ++k) dot = fmaf(Agt[k * K + i], Bt[k * K + jj], dot);
-            s = vals[jj] + dot;
+            for (int k = 0; k < kEmbed; k += 2) {
+                d0 = fmaf(Agt[k * K + i], Bt[k * K + jj], d0);
+                d1 = fmaf(Agt[(k + 1) * K + i], Bt[(k + 1) * K + jj], d1);
+            }
+            s = vals[jj] + (d0 + d1);
         } else {
             s = -INFINITY;  // only the anchor precedes position 0
         }
@@ -291,27 +317,39 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
     // ---------------- walk (one warp; lane j = candidate rank j)
     // The sequence's L tables (L * K * K floats <= 2 * 256 * K) replace the
     // projection tiles in shared memory; the other CTAs' writes are read
-    // around L1.
+    // around L1, 16 floats per thread per batch.
     float *const Pb = pw_smem;
     {
-        const float *src = p.P + static_cast<size_t>(b) * L * K * K;
-        for (int i = tid; i < L * K * K; i += blockDim.x) Pb[i] = __ldcg(src + i);
+        const float4 *src = reinterpret_cast<const float4 *>(p.P + static_cast<size_t>(b) * L * K * K);
+        float4 *dst = reinterpret_cast<float4 *>(Pb);
+        const int n4 = L * K * K / 4;
+        for (int i0 = 0; i0 < n4; i0 += 4 * 256) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * 256 + tid;
+                if (i < n4) v[u] = __ldcg(src + i);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * 256 + tid;
+                if (i < n4) dst[i] = v[u];
+            }
+        }
     }
     __syncthreads();
     if (tid >= 32) return;
     const int lane = tid;
     const bool active = lane < K;
-    int ranks[16];
     float score;
-    uint8_t flags[16];
-    for (int s = 0; s < L; ++s) flags[s] = 0;
 
     if (p.walk == 0) {
         float delta = active ? Pb[lane] : -INFINITY;
         for (int s = 1; s < L; ++s) {
             float best = -INFINITY, second = -INFINITY;
             int bi = 0;
-            const float *Ps = Pb + static_cast<size_t>(s) * K * K;
+            const float *Ps = Pb + s * K * K;
+#pragma unroll
             for (int i = 0; i < K; ++i) {
                 const float di = __shfl_sync(0xFFFFFFFFu, delta, i);
                 const float v = active ? di + Ps[i * K + lane] : -INFINITY;
@@ -324,8 +362,8 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
                 }
             }
             if (active) {
-                bp[s * 32 + lane] = static_cast<uint8_t>(bi);
-                mg[s * 32 + lane] = best - second;
+                bp[s * K + lane] = static_cast<uint8_t>(bi);
+                mg[s * K + lane] = best - second;
             }
             delta = best;
         }
@@ -344,15 +382,19 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
         for (int off = 16; off > 0; off >>= 1) sv = fmaxf(sv, __shfl_xor_sync(0xFFFFFFFFu, sv, off));
         __syncwarp();
         score = bv;
-        int jcur = bj;
-        for (int s = L - 1; s >= 0; --s) {
-            ranks[s] = jcur;
-            if (s > 0) {
-                if (mg[s * 32 + jcur] < p.tie_eps) flags[s] |= 1;
-                jcur = bp[s * 32 + jcur];
+        if (lane == 0) {
+            int jcur = bj;
+            for (int s = L - 1; s >= 0; --s) {
+                ranks_s[s] = jcur;
+                uint8_t f = 0;
+                if (s > 0) {
+                    if (mg[s * K + jcur] < p.tie_eps) f |= 1;
+                    jcur = bp[s * K + jcur];
+                }
+                if (s == L - 1 && bv - sv < p.tie_eps) f |= 2;
+                flags_s[s] = f;
             }
         }
-        if (bv - sv < p.tie_eps) flags[L - 1] |= 2;
     } else {
         int prev = 0;
         float total = 0.f;
@@ -370,24 +412,20 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
             }
             float sv = (active && lane != bj) ? v : -INFINITY;
             for (int off = 16; off > 0; off >>= 1) sv = fmaxf(sv, __shfl_xor_sync(0xFFFFFFFFu, sv, off));
-            ranks[s] = bj;
-            if (bv - sv < p.tie_eps) flags[s] |= 1;
+            if (lane == 0) {
+                ranks_s[s] = bj;
+                flags_s[s] = (bv - sv < p.tie_eps) ? 1 : 0;
+            }
             total += bv;
             prev = bj;
         }
         score = total;
     }
+    __syncwarp();
     if (lane < L) {
-        int rk = 0;
-        uint8_t fl = 0;
-        for (int s = 0; s < L; ++s)
-            if (s == lane) {
-                rk = ranks[s];
-                fl = flags[s];
-            }
         const size_t o = static_cast<size_t>(b) * L + lane;
-        p.path[o] = p.ids[o * K + rk];
-        if (p.tie_flags) p.tie_flags[o] = fl;
+        p.path[o] = p.ids[o * K + ranks_s[lane]];
+        if (p.tie_flags) p.tie_flags[o] = flags_s[lane];
     }
     if (lane == 0 && p.path_score) p.path_score[b] = score;
 }
@@ -406,7 +444,9 @@ cudaError_t prepare_pair_walk(int smem_optin)
 {
     cudaError_t e = set_max_dynamic_smem(projection_kernel, smem_optin);
     if (e != cudaSuccess) return e;
-    return set_max_dynamic_smem(pair_walk_kernel, smem_optin);
+    e = set_max_dynamic_smem(pair_walk_kernel<16>, smem_optin);
+    if (e != cudaSuccess) return e;
+    return set_max_dynamic_smem(pair_walk_kernel<32>, smem_optin);
 }
 
 cudaError_t launch_projection(const ProjParams &p, cudaStream_t s)
@@ -418,7 +458,8 @@ cudaError_t launch_projection(const ProjParams &p, cudaStream_t s)
 cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s)
 {
     const size_t smem = 2u * kEmbed * p.K * sizeof(float);
-    return launch_ex(pair_walk_kernel, dim3(p.B * p.L), dim3(256), smem, s, 1, p);
+    if (p.K == 16) return launch_ex(pair_walk_kernel<16>, dim3(p.B * p.L), dim3(256), smem, s, 1, p);
+    return launch_ex(pair_walk_kernel<32>, dim3(p.B * p.L), dim3(256), smem, s, 1, p);
 }
 
 }  // namespace dfl
