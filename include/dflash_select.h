@@ -145,6 +145,33 @@ dflash_status dflash_select_profile_read(dflash_select_handle h, double *ms_tota
 /* Number of kernel launches one dflash_select_run makes for batch B. */
 int32_t dflash_select_launches_per_run(dflash_select_handle h, int32_t B);
 
+/* The lm_head + top-K stage alone, for callers that must not allocate device
+ * memory (the paper has no counterpart: it is a deployment convenience). A
+ * selector handle owns a workspace that dflash_select_init allocates; some
+ * hosts cannot allow that, e.g. engines that own all device memory in a
+ * preallocated arena, or code paths where an allocation would synchronise the
+ * device. This call allocates nothing: its scratch is one fixed 4 MiB device
+ * array inside the library, present on every GPU that loads the library until
+ * the process exits.
+ *   W_lm      [V, d] bf16   lm_head weight (16-byte aligned)
+ *   hidden    [N, d] bf16   hidden states of N positions (16-byte aligned)
+ *   topk_ids  [N, K] int32  candidates, by logit descending then id ascending
+ *   topk_vals [N, K] fp32   their logits (NULL = not wanted)
+ *   device_status [1] int32 on the device (NULL = not wanted): 0, or the
+ *             device error bits (2 = a pipeline wait ran out of time)
+ * Limits: 1 <= N <= 256, K in {16, 32}, d % 64 == 0, and the partial lists
+ * (min(SMs, ceil(V / 128)) * N * K * 8 bytes) must fit in the scratch; larger
+ * shapes return DFLASH_ERR_UNSUPPORTED with the sizes in the message.
+ * The first call on a device looks up the scratch's address and sets kernel
+ * attributes for that device; make that first call before any stream capture.
+ * Every call on a device shares the one scratch array, which keeps the last
+ * call's contents; calls whose work overlaps on the GPU (different streams,
+ * or host threads racing on one device) corrupt each other's results, so
+ * order them on one stream. Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+dflash_status dflash_lmhead_topk_noalloc(const void *W_lm, int64_t V, int32_t d, const void *hidden, int32_t N,
+                                         int32_t K, int32_t *topk_ids, float *topk_vals, int32_t *device_status,
+                                         void *stream);
+
 /* Frees the workspace (after the device is idle) and the handle. Returns a
  * latched device error if one is pending, else DFLASH_OK. NULL is a no-op. */
 dflash_status dflash_select_destroy(dflash_select_handle h);

@@ -68,10 +68,11 @@ def lib() -> ctypes.CDLL:
             L.dflash_select_launches_per_run.argtypes = [P, i32]
             L.dflash_select_launches_per_run.restype = i32
             L.dflash_select_destroy.argtypes = [P]
+            L.dflash_lmhead_topk_noalloc.argtypes = [P, i64, i32, P, i32, i32, P, P, P, P]
             L.dflash_last_error.restype = ctypes.c_char_p
             for f in ("dflash_select_init", "dflash_select_run", "dflash_verify_prefix", "dflash_select_step_host",
                       "dflash_select_sync_status", "dflash_select_profile", "dflash_select_profile_read",
-                      "dflash_select_destroy"):
+                      "dflash_select_destroy", "dflash_lmhead_topk_noalloc"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -216,6 +217,22 @@ def bind_step(handle, hidden, anchor, path, target=None, accept_len=None, emitte
         if st:
             _check(st, "dflash_verify_prefix")
     return step
+
+
+def dflash_lmhead_topk_noalloc(W, hidden, K, topk_ids, topk_vals=None, device_status=None, stream=None):
+    """lm_head + top-K of hidden [N, d] against W [V, d] (bf16, device) into
+    topk_ids [N, K] (and topk_vals) without any device allocation: the library
+    keeps a fixed scratch array per GPU. Calls on one GPU must not overlap."""
+    import torch
+    V, d = W.shape
+    N = hidden.shape[0]
+    if hidden.dim() != 2 or hidden.shape[1] != d:
+        raise ValueError("hidden must be [N, d]")
+    _check(lib().dflash_lmhead_topk_noalloc(_ptr(W, torch.bfloat16, "W"), V, d, _ptr(hidden, torch.bfloat16, "hidden"),
+                                            N, K, _ptr(topk_ids, torch.int32, "topk_ids"),
+                                            _ptr(topk_vals, torch.float32, "topk_vals"),
+                                            _ptr(device_status, torch.int32, "device_status"), _stream(stream)),
+           "dflash_lmhead_topk_noalloc")
 
 
 def dflash_select_destroy(handle):

@@ -85,6 +85,25 @@ dflash_status make_tmap(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t 
     return ok();
 }
 
+}  // namespace
+
+namespace dfl {
+
+// Used by the other host translation units of the library.
+dflash_status host_fail(dflash_status st, const char *msg)
+{
+    return fail(st, "%s", msg);
+}
+
+dflash_status host_make_tmap(CUtensorMap *tm, const void *ptr, int64_t rows, int64_t cols, int box_rows)
+{
+    return make_tmap(tm, ptr, rows, cols, box_rows);
+}
+
+}  // namespace dfl
+
+namespace {
+
 constexpr int kProfileRuns = 4096;
 constexpr int kProfileKernels = 4;
 
