@@ -55,6 +55,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest value of x over all ranks (gloo all-reduce of one float);
+    x itself when running alone."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(B: int, world: int, steps: int, max_ms: float) -> float:
+    """Blocks per second of all replicas together: every rank ran `steps`
+    steps of B sequences; the job took as long as its slowest rank."""
+    return world * B * steps / (max_ms / 1e3)
+
+
 def hbm_peak():
     try:
         with open(PEAKS_FILE) as f:
@@ -300,10 +318,7 @@ def run_ours(args):
     prof = pkg.dflash_select_profile_read(sel.h)
     pkg.dflash_select_profile(sel.h, False)
     pkg.dflash_select_sync_status(sel.h, stream=stream)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
 
     # end to end through the host-buffer entry point: pinned inputs in, results out, every step
     hid_h = inp.hidden.pin_memory()
@@ -320,10 +335,7 @@ def run_ours(args):
     for _ in range(args.e2e_steps):
         pkg.dflash_select_step_host(sel.h, hid_h, anc_h, tgt_h, path_h, acc_h, em_h, stream=stream)
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, world)
     h2d = hid_h.numel() * 2 + anc_h.numel() * 4 + tgt_h.numel() * 4
     d2h = path_h.numel() * 4 + acc_h.numel() * 4 + em_h.numel() * 4 + 4
 
@@ -340,7 +352,7 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     achieved = k1_bytes / k1_avg_s / 1e9
     step_s = ms / 1e3 / args.steps
-    value = world * w.B / step_s
+    value = whole_job_value(w.B, world, args.steps, ms)
     sel.close()
 
     if rank == 0:
@@ -361,7 +373,7 @@ def run_ours(args):
                          "launches_timed": k1_n},
             "kernels_avg_us": {k: v[0] / max(1, v[1]) * 1e3 for k, v in prof.items()},
             "clocks": clk,
-            "e2e": {"value": world * w.B * args.e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": whole_job_value(w.B, world, args.e2e_steps, e2e_s * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                     "api": "dflash_select_step_host (pinned host buffers, copies and sync inside)"},
             "gpu_launches": launches_per_step * args.steps,
