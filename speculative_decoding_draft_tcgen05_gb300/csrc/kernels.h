@@ -65,7 +65,10 @@ cudaError_t prepare_pair_walk(int smem_optin);
 constexpr int kLmTileM = 128;   // vocabulary rows per MMA tile (TMEM lanes)
 constexpr int kLmTileK = 64;    // hidden columns per pipeline stage (128 B rows)
 constexpr int kLmThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kLmMaxStages = 8;
+#ifndef DFL_LM_MAX_STAGES
+#define DFL_LM_MAX_STAGES 8
+#endif
+constexpr int kLmMaxStages = DFL_LM_MAX_STAGES;  // TMA ring depth cap (shared memory permitting)
 
 struct LmHeadParams {
     CUtensorMap tm_w;     // lm_head W [V, d] bf16, box 64 x 128, 128B swizzle
