@@ -135,9 +135,10 @@ dflash_status dflash_select_sync_status(dflash_select_handle h, void *stream);
 dflash_status dflash_select_profile(dflash_select_handle h, int32_t enable);
 
 /* Reads the record: for kernel index k (0 = lm_head+top-K, 1 = merge,
- * 2 = projection, 3 = pair tables + walk), total milliseconds and launch
- * count over the recorded runs (at most 4096 runs are recorded). Waits for
- * the recorded events. n_kernels receives the number of kernel indices. */
+ * 2 = projection, 3 = pair tables + walk, 4 = the fused small-batch tail that
+ * replaces 1..3), total milliseconds and launch count over the recorded runs
+ * (at most 4096 runs are recorded). Waits for the recorded events.
+ * n_kernels receives the number of kernel indices. */
 dflash_status dflash_select_profile_read(dflash_select_handle h, double *ms_total,
                                          int64_t *launches, int32_t max_kernels,
                                          int32_t *n_kernels);

@@ -28,7 +28,7 @@ STATUS_NAMES = {0: "DFLASH_OK", 1: "DFLASH_ERR_INVALID_ARG", 2: "DFLASH_ERR_UNSU
 DFLASH_WALK_VITERBI = 0
 DFLASH_WALK_GREEDY = 1
 
-KERNEL_NAMES = ("lmhead_topk", "topk_merge", "projection", "pair_walk")
+KERNEL_NAMES = ("lmhead_topk", "topk_merge", "projection", "pair_walk", "select_tail")
 
 
 class DflashError(RuntimeError):

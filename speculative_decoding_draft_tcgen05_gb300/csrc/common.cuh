@@ -291,6 +291,24 @@ __device__ __forceinline__ uint64_t list_insert(uint64_t mine, uint64_t x, int l
     return mine;
 }
 
+// Bitonic sort of one key per lane across the warp, descending (lane 0 gets
+// the largest).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t x, int lane)
+{
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t o = shfl_xor_u64(x, j);
+            const bool descending_block = (lane & k) == 0;
+            const bool lower = (lane & j) == 0;
+            const bool keep_max = lower == descending_block;
+            x = keep_max ? (x > o ? x : o) : (x < o ? x : o);
+        }
+    }
+    return x;
+}
+
 // Merges two warp-distributed sorted lists (descending, K <= 32 entries in
 // lanes 0..K-1, K a power of two) and returns the K largest keys of the
 // union, sorted: max(a[i], b[K-1-i]) is a bitonic sequence holding exactly

@@ -105,11 +105,20 @@ dflash_status host_make_tmap(CUtensorMap *tm, const void *ptr, int64_t rows, int
 namespace {
 
 constexpr int kProfileRuns = 4096;
-constexpr int kProfileKernels = 4;
+constexpr int kProfileKernels = 5;  // lm_head+top-K, merge, projection, pair+walk, fused tail
+constexpr int kProfileSlots = 4;    // launches recorded per run
 
 struct Plan {
     int N, NT, n_tiles_n, G, grid, stages, R_total, ksplit;
     size_t smem;
+    bool fused_tail;  // one clustered kernel for merge + projections + tables + walk
+    int tail_cs, tail_S;
+    size_t tail_smem;
+};
+
+struct ProfRun {
+    int kid[kProfileSlots];
+    int n;
 };
 
 }  // namespace
@@ -119,7 +128,7 @@ struct dflash_select_ctx {
     const void *W, *E, *WA, *WB, *WH;
     int device = 0, num_sms = 0;
     size_t smem_optin = 0;  // opt-in shared memory per block
-    CUtensorMap tm_w, tm_gate, tm_h;
+    CUtensorMap tm_w, tm_gate, tm_h, tm_wa, tm_wb;
     const void *h_ptr = nullptr;
     int h_rows = -1;
     int m_tiles_vocab = 0, m_tiles_total = 0, R = 0;
@@ -138,7 +147,8 @@ struct dflash_select_ctx {
 
     bool prof = false;
     int prof_runs = 0;
-    std::vector<cudaEvent_t> ev;  // kProfileRuns x (kProfileKernels + 1)
+    std::vector<cudaEvent_t> ev;  // kProfileRuns x kProfileSlots x {begin, end}
+    std::vector<ProfRun> prof_rec;
 
     Plan plan(int B) const
     {
@@ -160,6 +170,10 @@ struct dflash_select_ctx {
         p.smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, st);
         p.R_total = B * R;
         p.ksplit = dfl::projection_ksplit(cfg.d, p.R_total, num_sms);
+        p.tail_cs = dfl::tail_cluster_size(cfg.d);
+        p.tail_S = dfl::tail_stages(cfg.K, p.G, p.tail_cs, static_cast<int>(smem_optin));
+        p.fused_tail = p.n_tiles_n == 1 && p.N * p.tail_cs <= num_sms && p.tail_S > 0;
+        p.tail_smem = p.fused_tail ? dfl::tail_smem_bytes(cfg.K, p.tail_S, p.G, p.tail_cs) : 0;
         return p;
     }
 };
@@ -213,6 +227,7 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
 
     CUDA_TRY(dfl::prepare_lmhead(static_cast<int>(prop.sharedMemPerBlockOptin)));
     CUDA_TRY(dfl::prepare_pair_walk(static_cast<int>(prop.sharedMemPerBlockOptin)));
+    CUDA_TRY(dfl::prepare_tail(static_cast<int>(prop.sharedMemPerBlockOptin)));
 
     dflash_select_ctx *c = new (std::nothrow) dflash_select_ctx();
     if (!c) return fail(DFLASH_ERR_CUDA, "out of host memory");
@@ -230,7 +245,9 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     c->R = cfg->L * cfg->K + 1;
 
     if ((st = make_tmap(&c->tm_w, W_lm, cfg->V, cfg->d, dfl::kLmTileM)) != DFLASH_OK ||
-        (st = make_tmap(&c->tm_gate, W_H, dfl::kEmbed, cfg->d, dfl::kLmTileM)) != DFLASH_OK) {
+        (st = make_tmap(&c->tm_gate, W_H, dfl::kEmbed, cfg->d, dfl::kLmTileM)) != DFLASH_OK ||
+        (st = make_tmap(&c->tm_wa, W_A, dfl::kEmbed, cfg->d, dfl::kEmbed)) != DFLASH_OK ||
+        (st = make_tmap(&c->tm_wb, W_B, dfl::kEmbed, cfg->d, dfl::kEmbed)) != DFLASH_OK) {
         delete c;
         return st;
     }
@@ -302,14 +319,27 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
 static void prof_ensure(dflash_select_ctx *c)
 {
     if (!c->ev.empty()) return;
-    c->ev.resize(static_cast<size_t>(kProfileRuns) * (kProfileKernels + 1));
+    c->ev.resize(static_cast<size_t>(kProfileRuns) * kProfileSlots * 2);
     for (auto &x : c->ev) cudaEventCreate(&x);
+    c->prof_rec.resize(kProfileRuns);
 }
 
-static void prof_mark(dflash_select_ctx *c, int k, cudaStream_t s)
+static bool prof_on(dflash_select_ctx *c)
 {
-    if (c->prof && c->prof_runs < kProfileRuns)
-        cudaEventRecord(c->ev[static_cast<size_t>(c->prof_runs) * (kProfileKernels + 1) + k], s);
+    return c->prof && c->prof_runs < kProfileRuns;
+}
+
+static void prof_begin(dflash_select_ctx *c, int slot, cudaStream_t s)
+{
+    if (prof_on(c)) cudaEventRecord(c->ev[(static_cast<size_t>(c->prof_runs) * kProfileSlots + slot) * 2], s);
+}
+
+static void prof_end(dflash_select_ctx *c, int slot, int kid, cudaStream_t s)
+{
+    if (!prof_on(c)) return;
+    cudaEventRecord(c->ev[(static_cast<size_t>(c->prof_runs) * kProfileSlots + slot) * 2 + 1], s);
+    c->prof_rec[c->prof_runs].kid[slot] = kid;
+    c->prof_rec[c->prof_runs].n = slot + 1;
 }
 
 dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,
@@ -350,11 +380,47 @@ dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, cons
     lp.gate = c->gate;
     lp.err = c->err;
 
-    prof_mark(c, 0, s);
+    prof_begin(c, 0, s);
     CUDA_TRY(dfl::launch_lmhead_topk(lp, pl.grid, pl.smem, s));
-    prof_mark(c, 1, s);
+    prof_end(c, 0, 0, s);
+
+    if (pl.fused_tail) {
+        dfl::TailParams tp;
+        tp.tm_wa = c->tm_wa;
+        tp.tm_wb = c->tm_wb;
+        tp.part = c->part;
+        tp.gate = c->gate;
+        tp.E = static_cast<const uint16_t *>(c->E);
+        tp.anchor = anchor;
+        tp.ids = c->ids;
+        tp.vals = c->vals;
+        tp.ids_out = topk_ids;
+        tp.vals_out = topk_vals;
+        tp.P = c->P;
+        tp.P_out = pair_scores;
+        tp.ticket = c->ticket;
+        tp.path = path;
+        tp.path_score = path_score;
+        tp.tie_flags = tie_flags;
+        tp.err = c->err;
+        tp.V = c->cfg.V;
+        tp.d = c->cfg.d;
+        tp.L = c->cfg.L;
+        tp.G = pl.G;
+        tp.N = pl.N;
+        tp.cs = pl.tail_cs;
+        tp.walk = c->cfg.walk;
+        tp.tie_eps = c->cfg.tie_eps;
+        prof_begin(c, 1, s);
+        CUDA_TRY(dfl::launch_select_tail(tp, c->cfg.K, pl.tail_S, pl.tail_smem, s));
+        prof_end(c, 1, 4, s);
+        if (prof_on(c)) ++c->prof_runs;
+        return ok();
+    }
+
+    prof_begin(c, 1, s);
     CUDA_TRY(dfl::launch_topk_merge(c->part, pl.G, pl.N, c->cfg.K, c->ids, c->vals, topk_ids, topk_vals, s));
-    prof_mark(c, 2, s);
+    prof_end(c, 1, 1, s);
 
     dfl::ProjParams pp;
     pp.E = static_cast<const uint16_t *>(c->E);
@@ -372,8 +438,9 @@ dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, cons
     pp.R_total = pl.R_total;
     pp.ksplit = pl.ksplit;
     pp.kchunk = c->cfg.d / pl.ksplit;
+    prof_begin(c, 2, s);
     CUDA_TRY(dfl::launch_projection(pp, s));
-    prof_mark(c, 3, s);
+    prof_end(c, 2, 2, s);
 
     dfl::PairParams q;
     q.AB = c->AB;
@@ -392,9 +459,10 @@ dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, cons
     q.R = c->R;
     q.walk = c->cfg.walk;
     q.tie_eps = c->cfg.tie_eps;
+    prof_begin(c, 3, s);
     CUDA_TRY(dfl::launch_pair_walk(q, s));
-    prof_mark(c, 4, s);
-    if (c->prof && c->prof_runs < kProfileRuns) ++c->prof_runs;
+    prof_end(c, 3, 3, s);
+    if (prof_on(c)) ++c->prof_runs;
     return ok();
 }
 
@@ -476,13 +544,16 @@ dflash_status dflash_select_profile_read(dflash_select_handle h, double *ms_tota
         launches[k] = 0;
     }
     for (int r = 0; r < h->prof_runs; ++r) {
-        cudaEvent_t *e = &h->ev[static_cast<size_t>(r) * (kProfileKernels + 1)];
-        CUDA_TRY(cudaEventSynchronize(e[kProfileKernels]));
-        for (int k = 0; k < nk; ++k) {
+        const ProfRun &pr = h->prof_rec[r];
+        for (int slot = 0; slot < pr.n; ++slot) {
+            cudaEvent_t *e = &h->ev[(static_cast<size_t>(r) * kProfileSlots + slot) * 2];
+            CUDA_TRY(cudaEventSynchronize(e[1]));
             float ms = 0.f;
-            CUDA_TRY(cudaEventElapsedTime(&ms, e[k], e[k + 1]));
-            ms_total[k] += ms;
-            launches[k] += 1;
+            CUDA_TRY(cudaEventElapsedTime(&ms, e[0], e[1]));
+            if (pr.kid[slot] < nk) {
+                ms_total[pr.kid[slot]] += ms;
+                launches[pr.kid[slot]] += 1;
+            }
         }
     }
     *n_kernels = nk;
@@ -491,8 +562,8 @@ dflash_status dflash_select_profile_read(dflash_select_handle h, double *ms_tota
 
 int32_t dflash_select_launches_per_run(dflash_select_handle h, int32_t B)
 {
-    (void)h;
-    return B > 0 ? 4 : 0;
+    if (!h || B <= 0 || B > h->cfg.max_batch) return 0;
+    return h->plan(B).fused_tail ? 2 : 4;
 }
 
 dflash_status dflash_select_destroy(dflash_select_handle h)

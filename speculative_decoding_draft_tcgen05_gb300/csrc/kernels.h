@@ -119,6 +119,34 @@ struct PairParams {
 };
 cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s);
 
+// ---- fused tail for small batches: merge + projections + pair tables + walk ----
+struct TailParams {
+    CUtensorMap tm_wa, tm_wb;  // W_A, W_B [256, d] bf16, box 64 x 256, 128B swizzle
+    const uint64_t *part;      // [G][N][K] partial top-K keys
+    const float *gate;         // [N][256]
+    const uint16_t *E;         // [V, d] bf16 bits
+    const int32_t *anchor;     // [B]
+    int32_t *ids;              // [N][K] merged candidates (workspace)
+    float *vals;               // [N][K]
+    int32_t *ids_out;          // optional copies for the caller
+    float *vals_out;
+    float *P;                  // [N][K][K] tables (workspace)
+    float *P_out;              // optional
+    unsigned *ticket;          // [B]
+    int32_t *path;             // [B, L]
+    float *path_score;         // optional [B]
+    uint8_t *tie_flags;        // optional [B, L]
+    int *err;
+    int64_t V;
+    int d, L, G, N, cs, walk;
+    float tie_eps;
+};
+int tail_cluster_size(int d);
+int tail_stages(int K, int G, int cs, int smem_optin);
+size_t tail_smem_bytes(int K, int S, int G, int cs);
+cudaError_t prepare_tail(int smem_optin);
+cudaError_t launch_select_tail(const TailParams &p, int K, int S, size_t smem, cudaStream_t s);
+
 // ---- greedy accept check ----
 cudaError_t launch_verify(const int32_t *path, const int32_t *target, int B, int L, int32_t *accept,
                           int32_t *emitted, cudaStream_t s);

@@ -28,6 +28,9 @@ namespace {
 
 constexpr uint32_t kTileABytes = kLmTileM * kLmTileK * 2;  // 16 KB
 constexpr uint32_t kTransposeBytes = 16 * kLmTileM * 4;    // 16 columns x 128 rows fp32
+// Up to this many surviving keys per warp are inserted one by one; more are
+// sorted and merged (a sort + merge costs about as much as 6 to 8 inserts).
+constexpr int kInsertLimit = 6;
 
 __device__ __forceinline__ void named_bar_sync(int id, int n)
 {
@@ -271,14 +274,22 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                         const uint64_t key =
                             (id < p.V) ? make_key(T[cc * kLmTileM + r], static_cast<uint32_t>(id)) : 0ull;
                         unsigned surv = __ballot_sync(0xFFFFFFFFu, key > th);
+                        if (surv && !loaded) {
+                            mine = (lane < K) ? lists[col * K + lane] : 0ull;
+                            loaded = true;
+                        }
+                        if (__popc(surv) > kInsertLimit) {
+                            // many survivors (early tiles): sort the warp's keys and
+                            // fold their best K into the list with one merge
+                            const uint64_t x = warp_sort_desc((key > th) ? key : 0ull, lane);
+                            mine = list_merge(mine, x, lane, K);
+                            th = shfl_u64(mine, K - 1);
+                            surv = 0;
+                        }
                         while (surv) {
                             const int src = __ffs(surv) - 1;
                             surv &= surv - 1;
                             const uint64_t x = shfl_u64(key, src);
-                            if (!loaded) {
-                                mine = (lane < K) ? lists[col * K + lane] : 0ull;
-                                loaded = true;
-                            }
                             if (x > th) {
                                 mine = list_insert(mine, x, lane, K);
                                 th = shfl_u64(mine, K - 1);

@@ -21,6 +21,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "walk.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -247,10 +248,7 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
     float *const Agt = pw_smem;                // (A(prev_i) (.) g_t)[k] at [k * K + i]
     float *const Bt = pw_smem + kEmbed * K;    // B(c_{t,j})[k] at [k * K + j]
     __shared__ float vals[K];
-    __shared__ uint8_t bp[16 * K];             // back-pointers [t][j]
-    __shared__ float mg[16 * K];               // incoming margins [t][j]
-    __shared__ int ranks_s[16];
-    __shared__ uint8_t flags_s[16];
+    __shared__ WalkSmem<K> ws;
     __shared__ int is_last;
 
     pdl_trigger();
@@ -314,120 +312,10 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
     __syncthreads();
     if (!is_last) return;
 
-    // ---------------- walk (one warp; lane j = candidate rank j)
-    // The sequence's L tables (L * K * K floats <= 2 * 256 * K) replace the
-    // projection tiles in shared memory; the other CTAs' writes are read
-    // around L1, 16 floats per thread per batch.
-    float *const Pb = pw_smem;
-    {
-        const float4 *src = reinterpret_cast<const float4 *>(p.P + static_cast<size_t>(b) * L * K * K);
-        float4 *dst = reinterpret_cast<float4 *>(Pb);
-        const int n4 = L * K * K / 4;
-        for (int i0 = 0; i0 < n4; i0 += 4 * 256) {
-            float4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i0 + u * 256 + tid;
-                if (i < n4) v[u] = __ldcg(src + i);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i0 + u * 256 + tid;
-                if (i < n4) dst[i] = v[u];
-            }
-        }
-    }
-    __syncthreads();
-    if (tid >= 32) return;
-    const int lane = tid;
-    const bool active = lane < K;
-    float score;
-
-    if (p.walk == 0) {
-        float delta = active ? Pb[lane] : -INFINITY;
-        for (int s = 1; s < L; ++s) {
-            float best = -INFINITY, second = -INFINITY;
-            int bi = 0;
-            const float *Ps = Pb + s * K * K;
-#pragma unroll
-            for (int i = 0; i < K; ++i) {
-                const float di = __shfl_sync(0xFFFFFFFFu, delta, i);
-                const float v = active ? di + Ps[i * K + lane] : -INFINITY;
-                if (v > best) {
-                    second = best;
-                    best = v;
-                    bi = i;
-                } else if (v > second) {
-                    second = v;
-                }
-            }
-            if (active) {
-                bp[s * K + lane] = static_cast<uint8_t>(bi);
-                mg[s * K + lane] = best - second;
-            }
-            delta = best;
-        }
-        // final argmax, smallest rank on ties; and the runner-up value
-        float bv = active ? delta : -INFINITY;
-        int bj = lane;
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-            const int oj = __shfl_xor_sync(0xFFFFFFFFu, bj, off);
-            if (ov > bv || (ov == bv && oj < bj)) {
-                bv = ov;
-                bj = oj;
-            }
-        }
-        float sv = (active && lane != bj) ? delta : -INFINITY;
-        for (int off = 16; off > 0; off >>= 1) sv = fmaxf(sv, __shfl_xor_sync(0xFFFFFFFFu, sv, off));
-        __syncwarp();
-        score = bv;
-        if (lane == 0) {
-            int jcur = bj;
-            for (int s = L - 1; s >= 0; --s) {
-                ranks_s[s] = jcur;
-                uint8_t f = 0;
-                if (s > 0) {
-                    if (mg[s * K + jcur] < p.tie_eps) f |= 1;
-                    jcur = bp[s * K + jcur];
-                }
-                if (s == L - 1 && bv - sv < p.tie_eps) f |= 2;
-                flags_s[s] = f;
-            }
-        }
-    } else {
-        int prev = 0;
-        float total = 0.f;
-        for (int s = 0; s < L; ++s) {
-            const float v = active ? Pb[(s * K + prev) * K + lane] : -INFINITY;
-            float bv = v;
-            int bj = lane;
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-                const int oj = __shfl_xor_sync(0xFFFFFFFFu, bj, off);
-                if (ov > bv || (ov == bv && oj < bj)) {
-                    bv = ov;
-                    bj = oj;
-                }
-            }
-            float sv = (active && lane != bj) ? v : -INFINITY;
-            for (int off = 16; off > 0; off >>= 1) sv = fmaxf(sv, __shfl_xor_sync(0xFFFFFFFFu, sv, off));
-            if (lane == 0) {
-                ranks_s[s] = bj;
-                flags_s[s] = (bv - sv < p.tie_eps) ? 1 : 0;
-            }
-            total += bv;
-            prev = bj;
-        }
-        score = total;
-    }
-    __syncwarp();
-    if (lane < L) {
-        const size_t o = static_cast<size_t>(b) * L + lane;
-        p.path[o] = p.ids[o * K + ranks_s[lane]];
-        if (p.tie_flags) p.tie_flags[o] = flags_s[lane];
-    }
-    if (lane == 0 && p.path_score) p.path_score[b] = score;
+    walk_sequence<K>(p.P + static_cast<size_t>(b) * L * K * K, p.ids + static_cast<size_t>(b) * L * K, L, p.walk,
+                     p.tie_eps, pw_smem, ws, p.path + static_cast<size_t>(b) * L,
+                     p.path_score ? p.path_score + b : nullptr,
+                     p.tie_flags ? p.tie_flags + static_cast<size_t>(b) * L : nullptr);
 }
 
 }  // namespace

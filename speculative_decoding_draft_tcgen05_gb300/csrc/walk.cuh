@@ -1,0 +1,145 @@
+// The walk over one sequence's precomputed pair tables (blog "DFlash 2: Keep
+// Drafting Parallel", section "A Lightweight Path Selector": the only
+// sequential work is the final walk, starting from the last verified token).
+//
+// Max-sum (Viterbi) walk: delta_0(j) = S_0(x0, j);
+// delta_t(j) = max_i delta_{t-1}(i) + S_t(i, j), the smallest rank i winning
+// ties; the path ends at the best final rank (smallest on ties) and is read
+// back through the back-pointers. Greedy walk: from x0, the best successor at
+// every step (smallest rank on ties). One warp, lane j = candidate rank j.
+#pragma once
+
+#include "common.cuh"
+
+namespace dfl {
+
+template <int K>
+struct WalkSmem {
+    uint8_t bp[16 * K];  // back-pointers [t][j]
+    float mg[16 * K];    // gap between the best and second incoming value [t][j]
+    int ranks[16];
+    uint8_t flags[16];
+};
+
+// Called by every thread of a 256-thread CTA, uniformly. Stages the L tables
+// P_seq [L, K, K] (written by other CTAs of this or an earlier kernel; read
+// around L1) into shared memory Pb, walks them with warp 0 and writes the
+// path tokens ids_seq[t * K + rank_t], the path score and the tie flags
+// (bit 0: the choice at t had a margin below tie_eps; bit 1 at t = L-1: the
+// final choice did).
+template <int K>
+__device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t *ids_seq, int L, int walk,
+                                              float tie_eps, float *Pb, WalkSmem<K> &ws, int32_t *path_out,
+                                              float *score_out, uint8_t *flags_out)
+{
+    const int tid = threadIdx.x;
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(P_seq);
+        float4 *dst = reinterpret_cast<float4 *>(Pb);
+        const int n4 = L * K * K / 4;
+        for (int i0 = 0; i0 < n4; i0 += 4 * 256) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * 256 + tid;
+                if (i < n4) v[u] = __ldcg(src + i);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * 256 + tid;
+                if (i < n4) dst[i] = v[u];
+            }
+        }
+    }
+    __syncthreads();
+    if (tid >= 32) return;
+    const int lane = tid;
+    const bool active = lane < K;
+    float score;
+
+    if (walk == 0) {
+        float delta = active ? Pb[lane] : -INFINITY;
+        for (int s = 1; s < L; ++s) {
+            float best = -INFINITY, second = -INFINITY;
+            int bi = 0;
+            const float *Ps = Pb + s * K * K;
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                const float di = __shfl_sync(0xFFFFFFFFu, delta, i);
+                const float v = active ? di + Ps[i * K + lane] : -INFINITY;
+                if (v > best) {
+                    second = best;
+                    best = v;
+                    bi = i;
+                } else if (v > second) {
+                    second = v;
+                }
+            }
+            if (active) {
+                ws.bp[s * K + lane] = static_cast<uint8_t>(bi);
+                ws.mg[s * K + lane] = best - second;
+            }
+            delta = best;
+        }
+        float bv = active ? delta : -INFINITY;
+        int bj = lane;
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+            const int oj = __shfl_xor_sync(0xFFFFFFFFu, bj, off);
+            if (ov > bv || (ov == bv && oj < bj)) {
+                bv = ov;
+                bj = oj;
+            }
+        }
+        float sv = (active && lane != bj) ? delta : -INFINITY;
+        for (int off = 16; off > 0; off >>= 1) sv = fmaxf(sv, __shfl_xor_sync(0xFFFFFFFFu, sv, off));
+        __syncwarp();
+        score = bv;
+        if (lane == 0) {
+            int jcur = bj;
+            for (int s = L - 1; s >= 0; --s) {
+                ws.ranks[s] = jcur;
+                uint8_t f = 0;
+                if (s > 0) {
+                    if (ws.mg[s * K + jcur] < tie_eps) f |= 1;
+                    jcur = ws.bp[s * K + jcur];
+                }
+                if (s == L - 1 && bv - sv < tie_eps) f |= 2;
+                ws.flags[s] = f;
+            }
+        }
+    } else {
+        int prev = 0;
+        float total = 0.f;
+        for (int s = 0; s < L; ++s) {
+            const float v = active ? Pb[(s * K + prev) * K + lane] : -INFINITY;
+            float bv = v;
+            int bj = lane;
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+                const int oj = __shfl_xor_sync(0xFFFFFFFFu, bj, off);
+                if (ov > bv || (ov == bv && oj < bj)) {
+                    bv = ov;
+                    bj = oj;
+                }
+            }
+            float sv = (active && lane != bj) ? v : -INFINITY;
+            for (int off = 16; off > 0; off >>= 1) sv = fmaxf(sv, __shfl_xor_sync(0xFFFFFFFFu, sv, off));
+            if (lane == 0) {
+                ws.ranks[s] = bj;
+                ws.flags[s] = (bv - sv < tie_eps) ? 1 : 0;
+            }
+            total += bv;
+            prev = bj;
+        }
+        score = total;
+    }
+    __syncwarp();
+    if (lane < L) {
+        path_out[lane] = __ldcg(ids_seq + lane * K + ws.ranks[lane]);
+        if (flags_out) flags_out[lane] = ws.flags[lane];
+    }
+    if (lane == 0 && score_out) *score_out = score;
+}
+
+}  // namespace dfl
