@@ -195,11 +195,12 @@ def test_profile_records_kernels(pkg):
             sel.run(d["hidden"], d["anchor"], out=out)
         rec = pkg.dflash_select_profile_read(sel.h)
         pkg.dflash_select_profile(sel.h, False)
+        per_run = pkg.dflash_select_launches_per_run(sel.h, w.B)
     assert set(rec) == set(pkg.KERNEL_NAMES)
     launched = {name for name, (ms, n) in rec.items() if n}
     # the small batch takes the fused tail; larger ones the three-kernel tail
     assert launched in ({"lmhead_topk", "select_tail"}, {"lmhead_topk", "topk_merge", "projection", "pair_walk"})
-    assert pkg.dflash_select_launches_per_run(sel.h, w.B) == len(launched)
+    assert per_run == len(launched)
     for name in launched:
         ms, n = rec[name]
         assert n == 5 and ms > 0, name
