@@ -61,7 +61,7 @@ __host__ __device__ inline uint32_t tmem_cols_for(int NT)
 }
 
 struct Layout {
-    uint32_t stage_bytes, off_T, off_list, off_thr, off_bar, total;
+    uint32_t stage_bytes, off_T, off_list, off_thr, off_thrf, off_flags, off_bar, total;
 };
 
 __host__ __device__ inline Layout make_layout(int NT, int K, int stages)
@@ -71,7 +71,9 @@ __host__ __device__ inline Layout make_layout(int NT, int K, int stages)
     l.off_T = stages * l.stage_bytes;
     l.off_list = l.off_T + kTransposeBytes;
     l.off_thr = l.off_list + static_cast<uint32_t>(NT) * K * 8;
-    l.off_bar = l.off_thr + static_cast<uint32_t>(NT) * 8;
+    l.off_thrf = l.off_thr + static_cast<uint32_t>(NT) * 8;
+    l.off_flags = l.off_thrf + static_cast<uint32_t>(NT) * 4;
+    l.off_bar = l.off_flags + 16;
     // full[S], empty[S], tfull[2], tempty[2], drain, then tmem base + abort flag
     l.total = l.off_bar + 8u * (2u * stages + 5u) + 16u;
     return l;
@@ -89,6 +91,10 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     float *const T = reinterpret_cast<float *>(gbase + lay.off_T);
     uint64_t *const lists = reinterpret_cast<uint64_t *>(gbase + lay.off_list);
     uint64_t *const thr = reinterpret_cast<uint64_t *>(gbase + lay.off_thr);
+    // per position: the logit of the K-th best key so far (-inf until K are held)
+    float *const thr_f = reinterpret_cast<float *>(gbase + lay.off_thrf);
+    // per 16-column chunk: which columns have a surviving logit (3 rotating words)
+    volatile uint32_t *const chunk_flags = reinterpret_cast<volatile uint32_t *>(gbase + lay.off_flags);
     const uint32_t bar_full = base + lay.off_bar;
     const uint32_t bar_empty = bar_full + 8u * S;
     const uint32_t bar_tfull = bar_empty + 8u * S;
@@ -118,7 +124,11 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < NT * K; i += kLmThreads) lists[i] = 0;
-    for (int i = threadIdx.x; i < NT; i += kLmThreads) thr[i] = 0;
+    for (int i = threadIdx.x; i < NT; i += kLmThreads) {
+        thr[i] = 0;
+        thr_f[i] = -INFINITY;
+    }
+    if (threadIdx.x < 4) chunk_flags[threadIdx.x] = 0;
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tm_w);
         tma_prefetch_desc(&p.tm_gate);
@@ -233,6 +243,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         const int nvalid = min(NT, p.N - col_base);
         const int ncols16 = (nvalid + 15) & ~15;
         int j = 0;
+        int nchunk = 0;  // top-K chunks processed so far (selects the flag word)
         bool ok = true;
         for (int m = chunk; m < p.m_tiles_total; m += G, ++j) {
             const int a = j & 1;
@@ -258,16 +269,44 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     }
                     continue;
                 }
+                // Cheap filter first: a logit can only enter a list if it is
+                // above that position's K-th best so far. Tiles arrive in
+                // increasing vocabulary order, so an equal logit (larger id)
+                // never can. Chunks where nothing survives end here.
+                const int slot = nchunk % 3;
+                ++nchunk;
+                uint32_t mask = 0;
+                if (static_cast<int64_t>(row0) + row < p.V) {
+                    const float4 *tf4 = reinterpret_cast<const float4 *>(thr_f + c0);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float4 th4 = tf4[q4];
+                        mask |= (v[4 * q4 + 0] > th4.x ? 1u : 0u) << (4 * q4 + 0);
+                        mask |= (v[4 * q4 + 1] > th4.y ? 1u : 0u) << (4 * q4 + 1);
+                        mask |= (v[4 * q4 + 2] > th4.z ? 1u : 0u) << (4 * q4 + 2);
+                        mask |= (v[4 * q4 + 3] > th4.w ? 1u : 0u) << (4 * q4 + 3);
+                    }
+                    const int vcols = nvalid - c0;
+                    if (vcols < 16) mask &= (1u << vcols) - 1u;
+                }
+                mask = __reduce_or_sync(0xFFFFFFFFu, mask);
+                if (lane == 0 && mask) atomicOr(const_cast<uint32_t *>(&chunk_flags[slot]), mask);
+                named_bar_sync(1, 128);
+                const uint32_t flags = chunk_flags[slot];
+                // the word of the previous chunk is free again: every epilogue
+                // thread read it before arriving at the barrier above
+                if (threadIdx.x == 64) chunk_flags[(slot + 2) % 3] = 0;
+                if (flags == 0) continue;  // uniform: all read the same word
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) T[jj * kLmTileM + row] = v[jj];
                 named_bar_sync(1, 128);
                 for (int cc = ew; cc < 16; cc += 4) {
                     const int col = c0 + cc;
-                    if (col >= nvalid) continue;  // uniform across the warp
+                    if (col >= nvalid || !((flags >> cc) & 1u)) continue;  // uniform across the warp
                     uint64_t th = thr[col];
                     uint64_t mine = 0;
                     bool loaded = false;
-#pragma unroll
+#pragma unroll 1
                     for (int qq = 0; qq < 4; ++qq) {
                         const int r = qq * 32 + lane;
                         const int64_t id = static_cast<int64_t>(row0) + r;
@@ -298,7 +337,10 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     }
                     if (loaded) {
                         if (lane < K) lists[col * K + lane] = mine;
-                        if (lane == 0) thr[col] = th;
+                        if (lane == 0) {
+                            thr[col] = th;
+                            thr_f[col] = th ? key_val(th) : -INFINITY;
+                        }
                     }
                 }
                 named_bar_sync(1, 128);
