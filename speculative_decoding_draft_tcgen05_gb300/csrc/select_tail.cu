@@ -231,7 +231,14 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
         if (p.ids_out) p.ids_out[o] = cand[0][tid];
         if (p.vals_out) p.vals_out[o] = cand_val[tid];
     }
-    if (tid < 2 * K) rowtok[tid] = (tid < K) ? cand[1][tid] : cand[0][tid - K];
+    if (tid < 2 * K) {
+        int32_t tok = (tid < K) ? cand[1][tid] : cand[0][tid - K];
+        if (tok >= 0 && static_cast<int64_t>(tok) >= p.V) {  // never for keys the lm_head kernel wrote
+            atomicOr(p.err, DEV_ERR_TOKEN);
+            tok = 0;
+        }
+        rowtok[tid] = tok;
+    }
     __syncthreads();
 
     // ---------------- 2. partial projections over this CTA's slice of d
