@@ -135,6 +135,7 @@ struct dflash_select_ctx {
 
     void *ws = nullptr;
     uint64_t *part = nullptr;
+    uint64_t *thr_g = nullptr;  // per-position lm_head thresholds shared by the CTAs
     float *gate = nullptr, *vals = nullptr, *AB = nullptr, *P = nullptr;
     int32_t *ids = nullptr;
     unsigned *ticket = nullptr;
@@ -264,6 +265,7 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     size_t off = 0;
     const size_t o_part = off; off += up(part_elems * 8);
+    const size_t o_thrg = off; off += up(Nmax * 8);
     const size_t o_gate = off; off += up(Nmax * dfl::kEmbed * 4);
     const size_t o_ids = off; off += up(Nmax * cfg->K * 4);
     const size_t o_vals = off; off += up(Nmax * cfg->K * 4);
@@ -290,6 +292,7 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     }
     uint8_t *w = static_cast<uint8_t *>(c->ws);
     c->part = reinterpret_cast<uint64_t *>(w + o_part);
+    c->thr_g = reinterpret_cast<uint64_t *>(w + o_thrg);
     c->gate = reinterpret_cast<float *>(w + o_gate);
     c->ids = reinterpret_cast<int32_t *>(w + o_ids);
     c->vals = reinterpret_cast<float *>(w + o_vals);
@@ -378,6 +381,7 @@ dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, cons
     lp.stages = pl.stages;
     lp.part = c->part;
     lp.gate = c->gate;
+    lp.thr_g = c->thr_g;
     lp.err = c->err;
 
     prof_begin(c, 0, s);
@@ -389,6 +393,7 @@ dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, cons
         tp.tm_wa = c->tm_wa;
         tp.tm_wb = c->tm_wb;
         tp.part = c->part;
+        tp.thr_g = c->thr_g;
         tp.gate = c->gate;
         tp.E = static_cast<const uint16_t *>(c->E);
         tp.anchor = anchor;
@@ -419,7 +424,7 @@ dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, cons
     }
 
     prof_begin(c, 1, s);
-    CUDA_TRY(dfl::launch_topk_merge(c->part, pl.G, pl.N, c->cfg.K, c->ids, c->vals, topk_ids, topk_vals, s));
+    CUDA_TRY(dfl::launch_topk_merge(c->part, pl.G, pl.N, c->cfg.K, c->ids, c->vals, topk_ids, topk_vals, c->thr_g, s));
     prof_end(c, 1, 1, s);
 
     dfl::ProjParams pp;

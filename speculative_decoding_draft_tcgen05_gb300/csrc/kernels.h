@@ -64,7 +64,7 @@ cudaError_t prepare_pair_walk(int smem_optin);
 // ---- lm_head GEMM + streaming top-K (and the context gate g = W_H h) ----
 constexpr int kLmTileM = 128;   // vocabulary rows per MMA tile (TMEM lanes)
 constexpr int kLmTileK = 64;    // hidden columns per pipeline stage (128 B rows)
-constexpr int kLmThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kLmThreads = 320; // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue (TMEM), 6..9 list helpers
 #ifndef DFL_LM_MAX_STAGES
 #define DFL_LM_MAX_STAGES 8
 #endif
@@ -77,8 +77,9 @@ struct LmHeadParams {
     int64_t V;
     int d, N, NT, n_tiles_n, K;
     int m_tiles_vocab, m_tiles_total, ctas_per_ntile, stages;
-    uint64_t *part;  // [ctas_per_ntile][N][K] partial top-K keys
-    float *gate;     // [N][256] g_t = W_H h_t
+    uint64_t *part;   // [ctas_per_ntile][N][K] partial top-K keys
+    float *gate;      // [N][256] g_t = W_H h_t
+    uint64_t *thr_g;  // [N] best K-th key published by any CTA; zero on entry, reset by the consumer
     int *err;
 };
 
@@ -87,7 +88,7 @@ cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cud
 
 // Merges the partial lists of every CTA into the sorted top-K of each position.
 cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws,
-                              float *vals_ws, int32_t *ids_out, float *vals_out, cudaStream_t s);
+                              float *vals_ws, int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s);
 
 // ---- candidate projections A|B = [W_A; W_B] E[row] (mma.sync, cluster split-K) ----
 struct ProjParams {
@@ -123,6 +124,7 @@ cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s);
 struct TailParams {
     CUtensorMap tm_wa, tm_wb;  // W_A, W_B [256, d] bf16, box 64 x 256, 128B swizzle
     const uint64_t *part;      // [G][N][K] partial top-K keys
+    uint64_t *thr_g;           // [N] lm_head thresholds, reset here for the next pass
     const float *gate;         // [N][256]
     const uint16_t *E;         // [V, d] bf16 bits
     const int32_t *anchor;     // [B]

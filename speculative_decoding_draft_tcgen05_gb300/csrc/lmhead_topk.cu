@@ -236,9 +236,14 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         }
     } else {
         // ------------------------------------------------ epilogue
-        const int ew = warp - 2;           // 0..3: column share
-        const int q = warp & 3;            // TMEM lane quadrant this warp may read
-        const int row = q * 32 + lane;     // tile row owned by this thread
+        // Warps 2..5 read TMEM (warp w may only touch lane quadrant w % 4);
+        // warps 6..9 only help with the per-position list work. All eight
+        // meet at named barrier 1.
+        const bool tmem_warp = warp < 6;
+        const int ew = warp - 2;           // 0..7: column share
+        const int q = warp & 3;            // TMEM lane quadrant (TMEM warps)
+        const int row = q * 32 + lane;     // tile row owned by this thread (TMEM warps)
+        const int et = threadIdx.x - 64;   // 0..255 among the epilogue threads
         const int col_base = n_tile * NT;
         const int nvalid = min(NT, p.N - col_base);
         const int ncols16 = (nvalid + 15) & ~15;
@@ -248,59 +253,84 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         for (int m = chunk; m < p.m_tiles_total; m += G, ++j) {
             const int a = j & 1;
             const uint32_t u = static_cast<uint32_t>(j >> 1);
-            const bool got = mbar_wait(bar_tfull + 8u * a, u & 1u, abort_flag);
-            if (named_bar_or(1, 128, !got)) {
+            const bool gate = m >= p.m_tiles_vocab;
+            // the cross-CTA thresholds, fetched while the accumulator fills
+            uint64_t tg[2] = {0ull, 0ull};
+            if (!gate) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    if (et + h * 256 < nvalid)
+                        tg[h] = *reinterpret_cast<volatile const uint64_t *>(p.thr_g + col_base + et + h * 256);
+            }
+            const bool got = tmem_warp ? mbar_wait(bar_tfull + 8u * a, u & 1u, abort_flag) : true;
+            if (!gate) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = et + h * 256;
+                    if (c < nvalid && tg[h] > thr[c]) {
+                        thr[c] = tg[h];
+                        thr_f[c] = key_val(tg[h]);
+                    }
+                }
+            }
+            if (named_bar_or(1, 256, !got)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * NT);
-            const bool gate = m >= p.m_tiles_vocab;
             const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
             for (int c0 = 0; c0 < ncols16; c0 += 16) {
                 float v[16];
-                __syncwarp();
-                tmem_load16(taddr + static_cast<uint32_t>(c0), v);
+                if (tmem_warp) {
+                    __syncwarp();
+                    tmem_load16(taddr + static_cast<uint32_t>(c0), v);
+                }
                 if (gate) {
+                    if (tmem_warp) {
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int pos = col_base + c0 + jj;
-                        if (c0 + jj < nvalid) p.gate[static_cast<size_t>(pos) * kEmbed + row0 + row] = v[jj];
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int pos = col_base + c0 + jj;
+                            if (c0 + jj < nvalid) p.gate[static_cast<size_t>(pos) * kEmbed + row0 + row] = v[jj];
+                        }
                     }
                     continue;
                 }
                 // Cheap filter first: a logit can only enter a list if it is
-                // above that position's K-th best so far. Tiles arrive in
-                // increasing vocabulary order, so an equal logit (larger id)
-                // never can. Chunks where nothing survives end here.
+                // not below that position's threshold (the larger of this
+                // CTA's K-th best and the best K-th published by any CTA: at
+                // least K logits reach it). Exact ties are settled by the full
+                // key below. Chunks where nothing survives end here.
                 const int slot = nchunk % 3;
                 ++nchunk;
                 uint32_t mask = 0;
-                if (static_cast<int64_t>(row0) + row < p.V) {
+                if (tmem_warp && static_cast<int64_t>(row0) + row < p.V) {
                     const float4 *tf4 = reinterpret_cast<const float4 *>(thr_f + c0);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         const float4 th4 = tf4[q4];
-                        mask |= (v[4 * q4 + 0] > th4.x ? 1u : 0u) << (4 * q4 + 0);
-                        mask |= (v[4 * q4 + 1] > th4.y ? 1u : 0u) << (4 * q4 + 1);
-                        mask |= (v[4 * q4 + 2] > th4.z ? 1u : 0u) << (4 * q4 + 2);
-                        mask |= (v[4 * q4 + 3] > th4.w ? 1u : 0u) << (4 * q4 + 3);
+                        mask |= (v[4 * q4 + 0] >= th4.x ? 1u : 0u) << (4 * q4 + 0);
+                        mask |= (v[4 * q4 + 1] >= th4.y ? 1u : 0u) << (4 * q4 + 1);
+                        mask |= (v[4 * q4 + 2] >= th4.z ? 1u : 0u) << (4 * q4 + 2);
+                        mask |= (v[4 * q4 + 3] >= th4.w ? 1u : 0u) << (4 * q4 + 3);
                     }
                     const int vcols = nvalid - c0;
                     if (vcols < 16) mask &= (1u << vcols) - 1u;
                 }
                 mask = __reduce_or_sync(0xFFFFFFFFu, mask);
                 if (lane == 0 && mask) atomicOr(const_cast<uint32_t *>(&chunk_flags[slot]), mask);
-                named_bar_sync(1, 128);
+                named_bar_sync(1, 256);
                 const uint32_t flags = chunk_flags[slot];
                 // the word of the previous chunk is free again: every epilogue
                 // thread read it before arriving at the barrier above
                 if (threadIdx.x == 64) chunk_flags[(slot + 2) % 3] = 0;
                 if (flags == 0) continue;  // uniform: all read the same word
+                if (tmem_warp) {
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) T[jj * kLmTileM + row] = v[jj];
-                named_bar_sync(1, 128);
-                for (int cc = ew; cc < 16; cc += 4) {
+                    for (int jj = 0; jj < 16; ++jj) T[jj * kLmTileM + row] = v[jj];
+                }
+                named_bar_sync(1, 256);
+                for (int cc = ew; cc < 16; cc += 8) {
                     const int col = c0 + cc;
                     if (col >= nvalid || !((flags >> cc) & 1u)) continue;  // uniform across the warp
                     uint64_t th = thr[col];
@@ -322,7 +352,8 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                             // fold their best K into the list with one merge
                             const uint64_t x = warp_sort_desc((key > th) ? key : 0ull, lane);
                             mine = list_merge(mine, x, lane, K);
-                            th = shfl_u64(mine, K - 1);
+                            const uint64_t kth = shfl_u64(mine, K - 1);
+                            th = kth > th ? kth : th;
                             surv = 0;
                         }
                         while (surv) {
@@ -331,27 +362,33 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                             const uint64_t x = shfl_u64(key, src);
                             if (x > th) {
                                 mine = list_insert(mine, x, lane, K);
-                                th = shfl_u64(mine, K - 1);
+                                const uint64_t kth = shfl_u64(mine, K - 1);
+                                th = kth > th ? kth : th;
                             }
                         }
                     }
                     if (loaded) {
                         if (lane < K) lists[col * K + lane] = mine;
+                        const uint64_t kth = shfl_u64(mine, K - 1);
                         if (lane == 0) {
                             thr[col] = th;
                             thr_f[col] = th ? key_val(th) : -INFINITY;
+                            // publish this CTA's K-th best: K logits are at least that large
+                            if (kth) atomicMax(reinterpret_cast<unsigned long long *>(p.thr_g + col_base + col),
+                                               static_cast<unsigned long long>(kth));
                         }
                     }
                 }
-                named_bar_sync(1, 128);
+                named_bar_sync(1, 256);
             }
-            tc_fence_before_sync();
-            mbar_arrive(bar_tempty + 8u * a);
+            if (tmem_warp) {
+                tc_fence_before_sync();
+                mbar_arrive(bar_tempty + 8u * a);
+            }
         }
         if (!ok) atomicOr(p.err, DEV_ERR_TIMEOUT);
-        named_bar_sync(1, 128);
-        const int t0 = threadIdx.x - 64;
-        for (int i = t0; i < nvalid * K; i += 128) {
+        named_bar_sync(1, 256);
+        for (int i = et; i < nvalid * K; i += 256) {
             const int col = i / K;
             p.part[(static_cast<size_t>(chunk) * p.N + col_base + col) * K + (i % K)] = lists[i];
         }
@@ -374,13 +411,14 @@ constexpr int kMergeWarps = 16;
 __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint64_t *__restrict__ part, int G,
                                                                       int N, int K, int32_t *ids_ws,
                                                                       float *vals_ws, int32_t *ids_out,
-                                                                      float *vals_out)
+                                                                      float *vals_out, uint64_t *thr_g)
 {
     extern __shared__ uint64_t mlists[];  // [G][K]
     __shared__ uint64_t wl[kMergeWarps][32];
     pdl_trigger();
     pdl_wait();
     const int col = blockIdx.x;
+    if (threadIdx.x == 0) thr_g[col] = 0;  // ready for the next lm_head pass
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // every load of a batch is issued before any of them is stored, so the
     // batch costs one memory round trip
@@ -444,11 +482,11 @@ cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cud
 }
 
 cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws, float *vals_ws,
-                              int32_t *ids_out, float *vals_out, cudaStream_t s)
+                              int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s)
 {
     const size_t smem = static_cast<size_t>(G) * K * sizeof(uint64_t);
     return launch_ex(topk_merge_kernel, dim3(N), dim3(kMergeWarps * 32), smem, s, 1, part, G, N, K, ids_ws,
-                     vals_ws, ids_out, vals_out);
+                     vals_ws, ids_out, vals_out, thr_g);
 }
 
 }  // namespace dfl

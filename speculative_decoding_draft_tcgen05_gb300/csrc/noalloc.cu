@@ -6,11 +6,12 @@
 // strict memory budget, or code running where a cudaMalloc would synchronise
 // the device and is therefore forbidden. Such a caller cannot create a
 // selector handle (dflash_select_init allocates the workspace). This entry
-// point needs nothing but the caller's inputs and outputs: the scratch the
-// lm_head kernel uses (per-CTA partial top-K lists, an error word, and the
-// logit values when the caller does not want them) lives in one file-scope
-// device array of fixed size, created when the library's kernels are loaded
-// on a GPU and kept by that GPU until the process exits.
+// point needs nothing but the caller's inputs and outputs. The scratch the
+// lm_head kernel uses (per-CTA partial top-K lists, per-position thresholds,
+// an error word, and the logit values when the caller does not want them)
+// lives in one file-scope device array of fixed size, created when the
+// library's kernels are loaded on a GPU and kept by that GPU until the
+// process exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -29,7 +30,9 @@ namespace {
 
 constexpr size_t kScratchBytes = size_t(4) << 20;       // 4 MiB per GPU
 constexpr size_t kErrOffset = 0;                        // device error word
-constexpr size_t kValsOffset = 256;                     // fp32 [N <= 256][K <= 32]
+constexpr size_t kThrOffset = 256;                      // u64 thresholds [N <= 256]
+constexpr size_t kZeroBytes = kThrOffset + 256 * 8;     // what each call clears
+constexpr size_t kValsOffset = kZeroBytes;              // fp32 [N <= 256][K <= 32]
 constexpr size_t kPartOffset = kValsOffset + 256 * 32 * 4;
 constexpr size_t kPartBytes = kScratchBytes - kPartOffset;
 constexpr int kMaxPositions = 256;
@@ -141,16 +144,17 @@ extern "C" dflash_status dflash_lmhead_topk_noalloc(const void *W_lm, int64_t V,
     p.stages = stages;
     p.part = reinterpret_cast<uint64_t *>(dev.scratch + kPartOffset);
     p.gate = nullptr;
+    p.thr_g = reinterpret_cast<uint64_t *>(dev.scratch + kThrOffset);
     p.err = reinterpret_cast<int *>(dev.scratch + kErrOffset);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the error word is the only part of the scratch that must start at zero
-    if (cudaMemsetAsync(p.err, 0, sizeof(int), s) != cudaSuccess)
-        return fail(DFLASH_ERR_CUDA, "clearing the scratch error word failed");
+    // the error word and the per-position thresholds must start at zero
+    if (cudaMemsetAsync(dev.scratch, 0, kZeroBytes, s) != cudaSuccess)
+        return fail(DFLASH_ERR_CUDA, "clearing the scratch failed");
     cudaError_t e = dfl::launch_lmhead_topk(p, G, dfl::lmhead_smem_bytes(NT, K, stages), s);
     if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "lm_head kernel launch failed (error %lld)", e);
     float *vals = topk_vals ? topk_vals : reinterpret_cast<float *>(dev.scratch + kValsOffset);
-    e = dfl::launch_topk_merge(p.part, G, N, K, topk_ids, vals, nullptr, nullptr, s);
+    e = dfl::launch_topk_merge(p.part, G, N, K, topk_ids, vals, nullptr, nullptr, p.thr_g, s);
     if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "merge kernel launch failed (error %lld)", e);
     if (device_status &&
         cudaMemcpyAsync(device_status, p.err, sizeof(int), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
     const int g0 = rank * per;
     const int gn = max(0, min(G, g0 + per) - g0);
     if (tid < kEmbed) gs[tid] = p.gate[static_cast<size_t>(pos) * kEmbed + tid];
+    if (rank == 0 && tid == 0) p.thr_g[pos] = 0;  // ready for the next lm_head pass
     {
         const int total = nq * gn * K;
         constexpr int kBatch = 8;
