@@ -53,9 +53,19 @@ __device__ __forceinline__ bool named_bar_or(int id, int n, bool pred)
     return r != 0;
 }
 
+// Independent accumulation chains per tile. Consecutive MMAs into the same
+// accumulator wait for each other, so with few positions (narrow N) one chain
+// leaves the tensor pipe idle between MMAs; k-step k of a tile goes to chain
+// k mod C and the epilogue adds the C partial sums. Two tiles' worth (double
+// buffering) of C chains must fit the 512 TMEM columns.
+__host__ __device__ inline int acc_chains(int NT)
+{
+    return NT <= 64 ? 4 : (NT <= 128 ? 2 : 1);
+}
+
 __host__ __device__ inline uint32_t tmem_cols_for(int NT)
 {
-    uint32_t need = 2u * static_cast<uint32_t>(NT), c = 32;
+    uint32_t need = 2u * static_cast<uint32_t>(acc_chains(NT) * NT), c = 32;
     while (c < need) c <<= 1;
     return c;
 }
@@ -109,6 +119,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     const int G = p.ctas_per_ntile;
     const int KB = p.d / kLmTileK;
     const uint32_t tmem_cols = tmem_cols_for(NT);
+    const int C = acc_chains(NT);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * NT);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(a * C * NT);
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
@@ -223,8 +234,8 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     const uint32_t sb = sa + kTileABytes;
 #pragma unroll
                     for (int k = 0; k < kLmTileK / 16; ++k)
-                        umma_bf16(d_tmem, smem_desc_sw128(sa + 32u * k), smem_desc_sw128(sb + 32u * k), idesc,
-                                  (kb | k) != 0);
+                        umma_bf16(d_tmem + static_cast<uint32_t>((k % C) * NT), smem_desc_sw128(sa + 32u * k),
+                                  smem_desc_sw128(sb + 32u * k), idesc, (kb > 0 || k >= C) ? 1u : 0u);
                     umma_commit(bar_empty + 8u * s);  // frees the stage once these MMAs have read it
                 }
                 if (ok) umma_commit(bar_tfull + 8u * a);
@@ -278,13 +289,20 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                 break;
             }
             tc_fence_after_sync();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * NT);
+            const uint32_t taddr =
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * C * NT);
             const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
             for (int c0 = 0; c0 < ncols16; c0 += 16) {
                 float v[16];
                 if (tmem_warp) {
                     __syncwarp();
                     tmem_load16(taddr + static_cast<uint32_t>(c0), v);
+                    for (int c = 1; c < C; ++c) {  // the other chains' partial sums, in chain order
+                        float w[16];
+                        tmem_load16(taddr + static_cast<uint32_t>(c * NT + c0), w);
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) v[jj] += w[jj];
+                    }
                 }
                 if (gate) {
                     if (tmem_warp) {
