@@ -109,7 +109,7 @@ constexpr int kProfileKernels = 5;  // lm_head+top-K, merge, projection, pair+wa
 constexpr int kProfileSlots = 4;    // launches recorded per run
 
 struct Plan {
-    int N, NT, n_tiles_n, G, grid, stages, R_total, ksplit;
+    int N, NT, n_tiles_n, G, grid, stages, boxes, R_total, ksplit;
     size_t smem;
     bool fused_tail;  // one clustered kernel for merge + projections + tables + walk
     int tail_cs, tail_S;
@@ -162,13 +162,15 @@ struct dflash_select_ctx {
         if (g > m_tiles_total) g = m_tiles_total;
         p.G = g;
         p.grid = g * p.n_tiles_n;
-        const size_t fixed = dfl::lmhead_smem_bytes(p.NT, cfg.K, 0);
-        const size_t stage = static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 +
-                             static_cast<size_t>(p.NT) * dfl::kLmTileK * 2;
+        p.boxes = dfl::lmhead_boxes(cfg.d);
+        const size_t fixed = dfl::lmhead_smem_bytes(p.NT, cfg.K, 0, p.boxes);
+        const size_t stage = static_cast<size_t>(p.boxes) *
+                             (static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 +
+                              static_cast<size_t>(p.NT) * dfl::kLmTileK * 2);
         int st = static_cast<int>((smem_optin - fixed) / stage);
         if (st > dfl::kLmMaxStages) st = dfl::kLmMaxStages;
         p.stages = st;
-        p.smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, st);
+        p.smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, st, p.boxes);
         p.R_total = B * R;
         p.ksplit = dfl::projection_ksplit(cfg.d, p.R_total, num_sms);
         p.tail_cs = dfl::tail_cluster_size(cfg.d);
@@ -379,6 +381,7 @@ dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, cons
     lp.m_tiles_total = c->m_tiles_total;
     lp.ctas_per_ntile = pl.G;
     lp.stages = pl.stages;
+    lp.boxes = pl.boxes;
     lp.part = c->part;
     lp.gate = c->gate;
     lp.thr_g = c->thr_g;

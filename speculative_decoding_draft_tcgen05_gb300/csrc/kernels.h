@@ -77,13 +77,15 @@ struct LmHeadParams {
     int64_t V;
     int d, N, NT, n_tiles_n, K;
     int m_tiles_vocab, m_tiles_total, ctas_per_ntile, stages;
+    int boxes;        // 64-column TMA boxes per pipeline stage (d % (64 * boxes) == 0)
     uint64_t *part;   // [ctas_per_ntile][N][K] partial top-K keys
     float *gate;      // [N][256] g_t = W_H h_t
     uint64_t *thr_g;  // [N] best K-th key published by any CTA; zero on entry, reset by the consumer
     int *err;
 };
 
-size_t lmhead_smem_bytes(int NT, int K, int stages);
+size_t lmhead_smem_bytes(int NT, int K, int stages, int boxes);
+int lmhead_boxes(int d);
 cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s);
 
 // Merges the partial lists of every CTA into the sorted top-K of each position.

@@ -60,7 +60,12 @@ __device__ __forceinline__ bool named_bar_or(int id, int n, bool pred)
 // buffering) of C chains must fit the 512 TMEM columns.
 __host__ __device__ inline int acc_chains(int NT)
 {
-    return NT <= 64 ? 4 : (NT <= 128 ? 2 : 1);
+#ifdef DFL_LM_CHAINS
+    return NT * DFL_LM_CHAINS <= 256 ? DFL_LM_CHAINS : 1;
+#else
+    (void)NT;
+    return 1;  // measured: more chains do not speed up the weight stream at N <= 64
+#endif
 }
 
 __host__ __device__ inline uint32_t tmem_cols_for(int NT)
@@ -74,10 +79,10 @@ struct Layout {
     uint32_t stage_bytes, off_T, off_list, off_thr, off_thrf, off_flags, off_bar, total;
 };
 
-__host__ __device__ inline Layout make_layout(int NT, int K, int stages)
+__host__ __device__ inline Layout make_layout(int NT, int K, int stages, int boxes)
 {
     Layout l;
-    l.stage_bytes = kTileABytes + static_cast<uint32_t>(NT) * kLmTileK * 2;
+    l.stage_bytes = static_cast<uint32_t>(boxes) * (kTileABytes + static_cast<uint32_t>(NT) * kLmTileK * 2);
     l.off_T = stages * l.stage_bytes;
     l.off_list = l.off_T + kTransposeBytes;
     l.off_thr = l.off_list + static_cast<uint32_t>(NT) * K * 8;
@@ -97,7 +102,9 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     uint8_t *const gbase = smem_raw + (base - raw);
 
     const int NT = p.NT, K = p.K, S = p.stages;
-    const Layout lay = make_layout(NT, K, S);
+    const int BX = p.boxes;  // 64-column boxes per stage
+    const Layout lay = make_layout(NT, K, S, BX);
+    const uint32_t w_bytes = static_cast<uint32_t>(BX) * kTileABytes;  // weight part of a stage
     float *const T = reinterpret_cast<float *>(gbase + lay.off_T);
     uint64_t *const lists = reinterpret_cast<uint64_t *>(gbase + lay.off_list);
     uint64_t *const thr = reinterpret_cast<uint64_t *>(gbase + lay.off_thr);
@@ -117,7 +124,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     const int n_tile = blockIdx.x % p.n_tiles_n;
     const int chunk = blockIdx.x / p.n_tiles_n;
     const int G = p.ctas_per_ntile;
-    const int KB = p.d / kLmTileK;
+    const int KB = p.d / (kLmTileK * BX);
     const uint32_t tmem_cols = tmem_cols_for(NT);
     const int C = acc_chains(NT);
 
@@ -163,7 +170,11 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
+#ifdef DFL_LM_NOHINT
+            const uint64_t pol_w = l2_policy_evict_normal();
+#else
             const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+#endif
             const uint64_t pol_h = l2_policy_evict_last();   // hidden: re-read by every CTA
             const int n_my_tiles = (p.m_tiles_total - chunk + G - 1) / G;
             const int total = n_my_tiles * KB;
@@ -175,13 +186,15 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                 const bool gate = m >= p.m_tiles_vocab;
                 const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
                 mbar_arrive_expect_tx(bar_full + 8u * it, lay.stage_bytes);
-                tma_load_2d(base + it * lay.stage_bytes, gate ? &p.tm_gate : &p.tm_w, kb * kLmTileK, row0,
-                            bar_full + 8u * it, pol_w);
+                for (int bx = 0; bx < BX; ++bx)
+                    tma_load_2d(base + it * lay.stage_bytes + bx * kTileABytes, gate ? &p.tm_gate : &p.tm_w,
+                                (kb * BX + bx) * kLmTileK, row0, bar_full + 8u * it, pol_w);
             }
             pdl_wait();
             for (int it = 0; it < pre; ++it)
-                tma_load_2d(base + it * lay.stage_bytes + kTileABytes, &p.tm_h, (it % KB) * kLmTileK, n_tile * NT,
-                            bar_full + 8u * it, pol_h);
+                for (int bx = 0; bx < BX; ++bx)
+                    tma_load_2d(base + it * lay.stage_bytes + w_bytes + bx * NT * kLmTileK * 2, &p.tm_h,
+                                ((it % KB) * BX + bx) * kLmTileK, n_tile * NT, bar_full + 8u * it, pol_h);
             int it = pre;
             bool ok = true;
             for (; ok && it < total; ++it) {
@@ -197,8 +210,11 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                 }
                 const uint32_t sa = base + s * lay.stage_bytes;
                 mbar_arrive_expect_tx(bar_full + 8u * s, lay.stage_bytes);
-                tma_load_2d(sa, tma, kb * kLmTileK, row0, bar_full + 8u * s, pol_w);
-                tma_load_2d(sa + kTileABytes, &p.tm_h, kb * kLmTileK, n_tile * NT, bar_full + 8u * s, pol_h);
+                for (int bx = 0; bx < BX; ++bx)
+                    tma_load_2d(sa + bx * kTileABytes, tma, (kb * BX + bx) * kLmTileK, row0, bar_full + 8u * s, pol_w);
+                for (int bx = 0; bx < BX; ++bx)
+                    tma_load_2d(sa + w_bytes + bx * NT * kLmTileK * 2, &p.tm_h, (kb * BX + bx) * kLmTileK,
+                                n_tile * NT, bar_full + 8u * s, pol_h);
             }
             if (!ok) {
                 atomicOr(p.err, DEV_ERR_TIMEOUT);
@@ -231,11 +247,17 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     }
                     tc_fence_after_sync();
                     const uint32_t sa = base + s * lay.stage_bytes;
-                    const uint32_t sb = sa + kTileABytes;
+                    const uint32_t sb = sa + w_bytes;
+                    for (int bx = 0; bx < BX; ++bx) {
 #pragma unroll
-                    for (int k = 0; k < kLmTileK / 16; ++k)
-                        umma_bf16(d_tmem + static_cast<uint32_t>((k % C) * NT), smem_desc_sw128(sa + 32u * k),
-                                  smem_desc_sw128(sb + 32u * k), idesc, (kb > 0 || k >= C) ? 1u : 0u);
+                        for (int k = 0; k < kLmTileK / 16; ++k) {
+                            const int ks = bx * (kLmTileK / 16) + k;  // k-step within the stage
+                            umma_bf16(d_tmem + static_cast<uint32_t>((ks % C) * NT),
+                                      smem_desc_sw128(sa + bx * kTileABytes + 32u * k),
+                                      smem_desc_sw128(sb + bx * NT * kLmTileK * 2 + 32u * k), idesc,
+                                      (kb > 0 || ks >= C) ? 1u : 0u);
+                        }
+                    }
                     umma_commit(bar_empty + 8u * s);  // frees the stage once these MMAs have read it
                 }
                 if (ok) umma_commit(bar_tfull + 8u * a);
@@ -482,9 +504,20 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint
 
 }  // namespace
 
-size_t lmhead_smem_bytes(int NT, int K, int stages)
+size_t lmhead_smem_bytes(int NT, int K, int stages, int boxes)
 {
-    return static_cast<size_t>(make_layout(NT, K, stages).total) + 1024;  // + alignment slack
+    return static_cast<size_t>(make_layout(NT, K, stages, boxes).total) + 1024;  // + alignment slack
+}
+
+int lmhead_boxes(int d)
+{
+#ifdef DFL_LM_BOXES
+    int b = DFL_LM_BOXES;
+#else
+    int b = 1;
+#endif
+    while (b > 1 && d % (kLmTileK * b) != 0) --b;
+    return b;
 }
 
 cudaError_t prepare_lmhead(int smem_optin)

@@ -137,8 +137,10 @@ extern "C" dflash_status dflash_lmhead_topk_noalloc(const void *W_lm, int64_t V,
     p.m_tiles_vocab = m_tiles;
     p.m_tiles_total = m_tiles;
     p.ctas_per_ntile = G;
-    const size_t fixed = dfl::lmhead_smem_bytes(NT, K, 0);
-    const size_t stage = static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 + static_cast<size_t>(NT) * dfl::kLmTileK * 2;
+    p.boxes = dfl::lmhead_boxes(d);
+    const size_t fixed = dfl::lmhead_smem_bytes(NT, K, 0, p.boxes);
+    const size_t stage = static_cast<size_t>(p.boxes) *
+                         (static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 + static_cast<size_t>(NT) * dfl::kLmTileK * 2);
     int stages = static_cast<int>((static_cast<size_t>(dev.smem_optin) - fixed) / stage);
     if (stages > dfl::kLmMaxStages) stages = dfl::kLmMaxStages;
     p.stages = stages;
@@ -151,7 +153,7 @@ extern "C" dflash_status dflash_lmhead_topk_noalloc(const void *W_lm, int64_t V,
     // the error word and the per-position thresholds must start at zero
     if (cudaMemsetAsync(dev.scratch, 0, kZeroBytes, s) != cudaSuccess)
         return fail(DFLASH_ERR_CUDA, "clearing the scratch failed");
-    cudaError_t e = dfl::launch_lmhead_topk(p, G, dfl::lmhead_smem_bytes(NT, K, stages), s);
+    cudaError_t e = dfl::launch_lmhead_topk(p, G, dfl::lmhead_smem_bytes(NT, K, stages, p.boxes), s);
     if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "lm_head kernel launch failed (error %lld)", e);
     float *vals = topk_vals ? topk_vals : reinterpret_cast<float *>(dev.scratch + kValsOffset);
     e = dfl::launch_topk_merge(p.part, G, N, K, topk_ids, vals, nullptr, nullptr, p.thr_g, s);
