@@ -514,7 +514,9 @@ int lmhead_boxes(int d)
 #ifdef DFL_LM_BOXES
     int b = DFL_LM_BOXES;
 #else
-    int b = 1;
+    // measured on GB300: two boxes per stage (256 contiguous bytes of every
+    // weight row per request) stream the weight ~14% faster than one
+    int b = 2;
 #endif
     while (b > 1 && d % (kLmTileK * b) != 0) --b;
     return b;
