@@ -155,14 +155,21 @@ struct dflash_select_ctx {
     {
         Plan p;
         p.N = B * cfg.L;
-        p.NT = p.N <= 256 ? ((p.N + 15) / 16) * 16 : 256;
-        p.n_tiles_n = (p.N + p.NT - 1) / p.NT;
+        // position tiles of at most 128 up to 256 positions (the per-CTA top-K
+        // upkeep grows with the tile's width), 256 beyond
+        if (p.N <= 256) {
+            p.n_tiles_n = (p.N + 127) / 128;
+            p.NT = (((p.N + p.n_tiles_n - 1) / p.n_tiles_n) + 15) / 16 * 16;
+        } else {
+            p.NT = 256;
+            p.n_tiles_n = (p.N + 255) / 256;
+        }
         int g = num_sms / p.n_tiles_n;
         if (g < 1) g = 1;
         if (g > m_tiles_total) g = m_tiles_total;
         p.G = g;
         p.grid = g * p.n_tiles_n;
-        p.boxes = dfl::lmhead_boxes(cfg.d);
+        p.boxes = dfl::lmhead_boxes(cfg.d, p.NT);
         const size_t fixed = dfl::lmhead_smem_bytes(p.NT, cfg.K, 0, p.boxes);
         const size_t stage = static_cast<size_t>(p.boxes) *
                              (static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 +

@@ -85,7 +85,7 @@ struct LmHeadParams {
 };
 
 size_t lmhead_smem_bytes(int NT, int K, int stages, int boxes);
-int lmhead_boxes(int d);
+int lmhead_boxes(int d, int NT);
 cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s);
 
 // Merges the partial lists of every CTA into the sorted top-K of each position.

@@ -76,7 +76,7 @@ __host__ __device__ inline uint32_t tmem_cols_for(int NT)
 }
 
 struct Layout {
-    uint32_t stage_bytes, off_T, off_list, off_thr, off_thrf, off_flags, off_bar, total;
+    uint32_t stage_bytes, off_T, off_wscr, off_list, off_thr, off_thrf, off_flags, off_bar, total;
 };
 
 __host__ __device__ inline Layout make_layout(int NT, int K, int stages, int boxes)
@@ -84,7 +84,8 @@ __host__ __device__ inline Layout make_layout(int NT, int K, int stages, int box
     Layout l;
     l.stage_bytes = static_cast<uint32_t>(boxes) * (kTileABytes + static_cast<uint32_t>(NT) * kLmTileK * 2);
     l.off_T = stages * l.stage_bytes;
-    l.off_list = l.off_T + kTransposeBytes;
+    l.off_wscr = l.off_T + kTransposeBytes;
+    l.off_list = l.off_wscr + 8 * kLmTileM;  // eight epilogue warps x 128 row indices
     l.off_thr = l.off_list + static_cast<uint32_t>(NT) * K * 8;
     l.off_thrf = l.off_thr + static_cast<uint32_t>(NT) * 8;
     l.off_flags = l.off_thrf + static_cast<uint32_t>(NT) * 4;
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     const Layout lay = make_layout(NT, K, S, BX);
     const uint32_t w_bytes = static_cast<uint32_t>(BX) * kTileABytes;  // weight part of a stage
     float *const T = reinterpret_cast<float *>(gbase + lay.off_T);
+    uint8_t *const wscr = gbase + lay.off_wscr;
     uint64_t *const lists = reinterpret_cast<uint64_t *>(gbase + lay.off_list);
     uint64_t *const thr = reinterpret_cast<uint64_t *>(gbase + lay.off_thr);
     // per position: the logit of the K-th best key so far (-inf until K are held)
@@ -374,36 +376,59 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     const int col = c0 + cc;
                     if (col >= nvalid || !((flags >> cc) & 1u)) continue;  // uniform across the warp
                     uint64_t th = thr[col];
-                    uint64_t mine = 0;
-                    bool loaded = false;
-#pragma unroll 1
+                    // the column's 128 keys of this tile, four per lane
+                    uint64_t key[4];
+                    unsigned surv[4];
+                    int total = 0;
+#pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
                         const int r = qq * 32 + lane;
                         const int64_t id = static_cast<int64_t>(row0) + r;
-                        const uint64_t key =
-                            (id < p.V) ? make_key(T[cc * kLmTileM + r], static_cast<uint32_t>(id)) : 0ull;
-                        unsigned surv = __ballot_sync(0xFFFFFFFFu, key > th);
-                        if (surv && !loaded) {
-                            mine = (lane < K) ? lists[col * K + lane] : 0ull;
-                            loaded = true;
+                        key[qq] = (id < p.V) ? make_key(T[cc * kLmTileM + r], static_cast<uint32_t>(id)) : 0ull;
+                        surv[qq] = __ballot_sync(0xFFFFFFFFu, key[qq] > th);
+                        total += __popc(surv[qq]);
+                    }
+                    const bool loaded = total > 0;
+                    uint64_t mine = 0;
+                    if (loaded) mine = (lane < K) ? lists[col * K + lane] : 0ull;
+                    if (total > kInsertLimit) {
+                        // many survivors (early tiles): pack their tile rows densely
+                        // in this warp's scratch, then rebuild, sort 32 at a time
+                        // and merge each batch into the list
+                        uint8_t *const scr = wscr + (warp - 2) * kLmTileM;
+                        const unsigned lt = (1u << lane) - 1u;
+                        int base_i = 0;
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) {
+                            if (key[qq] > th) scr[base_i + __popc(surv[qq] & lt)] = static_cast<uint8_t>(qq * 32 + lane);
+                            base_i += __popc(surv[qq]);
                         }
-                        if (__popc(surv) > kInsertLimit) {
-                            // many survivors (early tiles): sort the warp's keys and
-                            // fold their best K into the list with one merge
-                            const uint64_t x = warp_sort_desc((key > th) ? key : 0ull, lane);
+                        __syncwarp();
+                        for (int b0 = 0; b0 < total; b0 += 32) {
+                            uint64_t x = 0ull;
+                            if (b0 + lane < total) {
+                                const int r = scr[b0 + lane];
+                                x = make_key(T[cc * kLmTileM + r], static_cast<uint32_t>(row0 + r));
+                            }
+                            x = warp_sort_desc(x, lane);
                             mine = list_merge(mine, x, lane, K);
-                            const uint64_t kth = shfl_u64(mine, K - 1);
-                            th = kth > th ? kth : th;
-                            surv = 0;
                         }
-                        while (surv) {
-                            const int src = __ffs(surv) - 1;
-                            surv &= surv - 1;
-                            const uint64_t x = shfl_u64(key, src);
-                            if (x > th) {
-                                mine = list_insert(mine, x, lane, K);
-                                const uint64_t kth = shfl_u64(mine, K - 1);
-                                th = kth > th ? kth : th;
+                        __syncwarp();
+                        const uint64_t kth = shfl_u64(mine, K - 1);
+                        th = kth > th ? kth : th;
+                    } else if (loaded) {
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) {
+                            unsigned sv = surv[qq];
+                            while (sv) {
+                                const int src = __ffs(sv) - 1;
+                                sv &= sv - 1;
+                                const uint64_t x = shfl_u64(key[qq], src);
+                                if (x > th) {
+                                    mine = list_insert(mine, x, lane, K);
+                                    const uint64_t kth = shfl_u64(mine, K - 1);
+                                    th = kth > th ? kth : th;
+                                }
                             }
                         }
                     }
@@ -509,14 +534,14 @@ size_t lmhead_smem_bytes(int NT, int K, int stages, int boxes)
     return static_cast<size_t>(make_layout(NT, K, stages, boxes).total) + 1024;  // + alignment slack
 }
 
-int lmhead_boxes(int d)
+int lmhead_boxes(int d, int NT)
 {
 #ifdef DFL_LM_BOXES
     int b = DFL_LM_BOXES;
 #else
     // measured on GB300: two boxes per stage (256 contiguous bytes of every
     // weight row per request) stream the weight ~14% faster than one
-    int b = 2;
+    int b = NT <= 128 ? 2 : 1;  // wide position tiles keep one box so three stages still fit
 #endif
     while (b > 1 && d % (kLmTileK * b) != 0) --b;
     return b;

@@ -137,7 +137,7 @@ extern "C" dflash_status dflash_lmhead_topk_noalloc(const void *W_lm, int64_t V,
     p.m_tiles_vocab = m_tiles;
     p.m_tiles_total = m_tiles;
     p.ctas_per_ntile = G;
-    p.boxes = dfl::lmhead_boxes(d);
+    p.boxes = dfl::lmhead_boxes(d, NT);
     const size_t fixed = dfl::lmhead_smem_bytes(NT, K, 0, p.boxes);
     const size_t stage = static_cast<size_t>(p.boxes) *
                          (static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 + static_cast<size_t>(NT) * dfl::kLmTileK * 2);
