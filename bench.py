@@ -400,7 +400,7 @@ def run_ours(args):
                           "traffic": committed_traffic(args.workload),
                           "algorithmic_bytes_per_launch": k1_bytes, "avg_launch_us": k1_avg_s * 1e6,
                           "launches_timed": k1_n}),
-            "kernels_avg_us": {k: v[0] / max(1, v[1]) * 1e3 for k, v in prof.items()},
+            "kernels_avg_us": {k: v[0] / v[1] * 1e3 for k, v in prof.items() if v[1]},
             "clocks": clk,
             "e2e": {"value": whole_job_value(w.B, world, args.e2e_steps, e2e_s * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
