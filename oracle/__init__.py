@@ -61,6 +61,9 @@ def _load():
             lib.oracle_select_given.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, i32, P,
                                                 ctypes.c_int32, P, P, P, P, P, P, P, P]
             lib.oracle_max_threads.restype = i32
+            lib.oracle_sample_walk.argtypes = [i32, i32, P, ctypes.c_double, P, P, P, P]
+            lib.oracle_verify_rejection.argtypes = [i32, i32, i64, P, P, P, P, P, ctypes.c_double, P, P, P]
+            lib.oracle_verify_rejection.restype = i32
             _lib = lib
     return _lib
 
@@ -198,3 +201,36 @@ def select_given(W_bits, E_bits, WA_bits, WB_bits, WH_bits, h_bits, anchor: int,
     out["score"] = float(out["score"][0])
     out["final_margin"] = float(out["final_margin"][0])
     return out
+
+
+def sample_walk(P, T: float, u):
+    """Sampling walk over tables P [L, K, K] with temperature T and uniforms u [L].
+    Returns (ranks [L], q [L, K] distributions drawn from, margins [L])."""
+    P = np.ascontiguousarray(P, dtype=np.float64)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    L, K, _ = P.shape
+    ranks = np.empty(L, np.int32)
+    q = np.empty((L, K), np.float64)
+    mg = np.empty(L, np.float64)
+    _load().oracle_sample_walk(L, K, _p(P), float(T), _p(u), _p(ranks), _p(q), _p(mg))
+    return ranks, q, mg
+
+
+def verify_rejection(path, ids, q, p, u_acc, u_res: float):
+    """Rejection-sampling verification. path [L], ids [L, K], q [L, K] draft
+    probabilities, p [L+1, V] target probabilities, u_acc [L], u_res.
+    Returns (n, emitted [L+1], acceptance margins [L], draw margin)."""
+    path = np.ascontiguousarray(path, dtype=np.int32)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    u_acc = np.ascontiguousarray(u_acc, dtype=np.float64)
+    L, K = ids.shape
+    V = p.shape[1]
+    assert p.shape[0] == L + 1
+    emitted = np.empty(L + 1, np.int32)
+    am = np.empty(L, np.float64)
+    rm = np.empty(1, np.float64)
+    n = _load().oracle_verify_rejection(L, K, V, _p(path), _p(ids), _p(q), _p(p), _p(u_acc), float(u_res),
+                                        _p(emitted), _p(am), _p(rm))
+    return int(n), emitted, am, float(rm[0])

@@ -320,3 +320,120 @@ int oracle_max_threads(void)
     return 1;
 #endif
 }
+
+/* ---------------------------------------------------------------------------
+ * Sampling (temperature T > 0). Blog "DFlash 2: Keep Drafting Parallel",
+ * section "A Lightweight Path Selector": sampling draws from the same pair
+ * scores, and rejection sampling at verification restores the exact target
+ * distribution. Readings (listed in the design notes):
+ *   S1  the draft distribution at step t is the softmax over the K candidate
+ *       ranks of P[t, prev, .] / T, prev = the rank chosen at t-1 (row 0 at
+ *       t = 0), and the step draws by inverting its CDF in rank order with a
+ *       given uniform u_t: the first rank whose running sum exceeds u_t;
+ *   S2  verification accepts draft token x_t with probability
+ *       min(1, p_t(x_t) / q_t(x_t)) (uniform u_acc_t below it accepts); at the
+ *       first rejection it draws from the residual max(0, p_t - q_t),
+ *       normalised, by inverting its CDF in vocabulary order with u_res; if all
+ *       L drafts are accepted it draws the bonus token from p_L the same way.
+ * Uniform random numbers are inputs.
+ * ------------------------------------------------------------------------- */
+
+/* ranks [L], q_all [L, K] (the distribution drawn from at each step),
+ * margin [L] = distance of u_t to the nearest CDF boundary of its step. */
+void oracle_sample_walk(int L, int K, const double *P, double T, const double *u, int32_t *ranks, double *q_all,
+                        double *margin)
+{
+    int prev = 0;
+    for (int t = 0; t < L; ++t) {
+        const double *row = P + ((int64_t)t * K + prev) * K;
+        double m = -INFINITY;
+        for (int j = 0; j < K; ++j)
+            if (row[j] > m) m = row[j];
+        double Z = 0.0;
+        double *q = q_all + (int64_t)t * K;
+        for (int j = 0; j < K; ++j) {
+            q[j] = exp((row[j] - m) / T);
+            Z += q[j];
+        }
+        for (int j = 0; j < K; ++j) q[j] /= Z;
+        double c = 0.0, mg = INFINITY;
+        int chosen = -1;
+        for (int j = 0; j < K; ++j) {
+            c += q[j];
+            const double dist = fabs(c - u[t]);
+            if (j < K - 1 && dist < mg) mg = dist;
+            if (chosen < 0 && c > u[t]) chosen = j;
+        }
+        if (chosen < 0) chosen = K - 1;  /* u within rounding of 1 */
+        ranks[t] = chosen;
+        margin[t] = mg;
+        prev = chosen;
+    }
+}
+
+/* Draws from the distribution r (length V, total Z > 0) with uniform u:
+ * the first index whose running sum exceeds u * Z. *margin receives the
+ * smallest distance, as a fraction of Z, between u and a CDF boundary. */
+static int64_t draw_inverse_cdf(const double *r, int64_t V, double u, double *margin)
+{
+    double Z = 0.0;
+    for (int64_t y = 0; y < V; ++y) Z += r[y];
+    const double target = u * Z;
+    double c = 0.0, mg = INFINITY;
+    int64_t chosen = -1, last = 0;
+    for (int64_t y = 0; y < V; ++y) {
+        if (r[y] <= 0.0) continue;
+        last = y;
+        c += r[y];
+        const double dist = fabs(c - target) / Z;
+        if (dist < mg && c < Z) mg = dist;
+        if (chosen < 0 && c > target) chosen = y;
+    }
+    if (chosen < 0) chosen = last;
+    *margin = mg;
+    return chosen;
+}
+
+/* Rejection-sampling verification of one sampled draft.
+ * path [L] draft tokens, ids [L, K] candidates, q [L, K] their draft
+ * probabilities, p [L+1, V] target probabilities, u_acc [L], u_res.
+ * Returns n (accepted drafts); emitted [L+1] = path[0..n-1], then the drawn
+ * token, then -1. acc_margin[t] = |u_acc[t] - min(1, p/q)| for the decided
+ * positions (+inf after the stop); res_margin = the draw's CDF margin. */
+int oracle_verify_rejection(int L, int K, int64_t V, const int32_t *path, const int32_t *ids, const double *q,
+                            const double *p, const double *u_acc, double u_res, int32_t *emitted,
+                            double *acc_margin, double *res_margin)
+{
+    double *r = (double *)malloc((size_t)V * sizeof(double));
+    int n = 0;
+    for (int t = 0; t < L; ++t) acc_margin[t] = INFINITY;
+    for (; n < L; ++n) {
+        const int32_t x = path[n];
+        double qx = 0.0;
+        for (int j = 0; j < K; ++j)
+            if (ids[n * K + j] == x) qx = q[n * K + j];
+        const double px = p[(int64_t)n * V + x];
+        const double a = (qx > 0.0) ? fmin(1.0, px / qx) : 0.0;
+        acc_margin[n] = fabs(u_acc[n] - a);
+        if (!(u_acc[n] < a)) break;
+    }
+    for (int t = 0; t < n; ++t) emitted[t] = path[t];
+    const double *pt = p + (int64_t)n * V;
+    if (n < L) {
+        for (int64_t y = 0; y < V; ++y) r[y] = pt[y];
+        for (int j = 0; j < K; ++j) {
+            const int32_t c = ids[n * K + j];
+            r[c] = fmax(0.0, pt[c] - q[n * K + j]);
+        }
+        double Z = 0.0;
+        for (int64_t y = 0; y < V; ++y) Z += r[y];
+        if (!(Z > 0.0))
+            for (int64_t y = 0; y < V; ++y) r[y] = pt[y];
+    } else {
+        for (int64_t y = 0; y < V; ++y) r[y] = pt[y];
+    }
+    emitted[n] = (int32_t)draw_inverse_cdf(r, V, u_res, res_margin);
+    for (int t = n + 1; t <= L; ++t) emitted[t] = -1;
+    free(r);
+    return n;
+}
