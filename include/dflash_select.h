@@ -54,7 +54,9 @@ typedef enum {
 
 typedef enum {
     DFLASH_WALK_VITERBI = 0,  /* max-sum walk over the pair tables */
-    DFLASH_WALK_GREEDY = 1    /* from x0, follow the best successor at each step */
+    DFLASH_WALK_GREEDY = 1,   /* from x0, follow the best successor at each step */
+    DFLASH_WALK_SAMPLE = 2    /* from x0, draw each step from softmax(S_t(prev, .) / temperature)
+                                 (dflash_select_run_sampled only) */
 } dflash_walk;
 
 /* Shapes fixed for the lifetime of a handle.
@@ -69,6 +71,7 @@ typedef struct {
     int32_t max_batch;  /* largest batch any run will pass; sizes the workspace */
     int32_t walk;       /* dflash_walk */
     float tie_eps;      /* margin under which tie_flags are raised, e.g. 1e-3 */
+    float temperature;  /* > 0; used by DFLASH_WALK_SAMPLE */
 } dflash_select_config;
 
 typedef struct dflash_select_ctx *dflash_select_handle;
@@ -102,6 +105,42 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
 dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, const int32_t *anchor,
                                 int32_t B, int32_t *topk_ids, float *topk_vals, float *pair_scores,
                                 int32_t *path, float *path_score, uint8_t *tie_flags, void *stream);
+
+/* The selector with the sampling walk (handle created with walk =
+ * DFLASH_WALK_SAMPLE). Blog "DFlash 2: Keep Drafting Parallel", section "A
+ * Lightweight Path Selector": sampling draws from the same pair scores. At
+ * every position the next candidate rank is drawn from
+ * softmax(S_t(prev, .) / temperature) over the K candidates (prev = the rank
+ * drawn at t-1, x0 at t = 0) by inverting the distribution's CDF in rank
+ * order with the given uniform.
+ *   u_walk      [B, L] fp32 uniforms in [0, 1)
+ *   draft_probs [B, L, K] fp32 output: the distribution drawn from at each t
+ *               (over the candidates in topk_ids order); needed by
+ *               dflash_verify_rejection
+ * Other arguments, outputs and errors as dflash_select_run; tie_flags bit 0
+ * marks a uniform within tie_eps of a CDF boundary. */
+dflash_status dflash_select_run_sampled(dflash_select_handle h, const void *hidden, const int32_t *anchor,
+                                        int32_t B, const float *u_walk, int32_t *topk_ids, float *topk_vals,
+                                        float *pair_scores, int32_t *path, float *draft_probs,
+                                        float *path_score, uint8_t *tie_flags, void *stream);
+
+/* Rejection-sampling verification of a sampled draft (same section: rejection
+ * sampling restores the exact target distribution). Draft token path[t] is
+ * kept when u_acc[t] < min(1, p_t(x) / q_t(x)); at the first rejection the
+ * emitted token is drawn from max(0, p_t - q_t) normalised (q_t is zero off
+ * the candidates), by inverting its CDF in vocabulary order with u_res; when
+ * all L drafts are kept the bonus token is drawn from p_L the same way.
+ *   path [B, L] int32, topk_ids [B, L, K] int32, draft_probs [B, L, K] fp32
+ *   (as written by dflash_select_run_sampled)
+ *   target_probs [B, L+1, V] fp32  target distribution after x0, path[0], ...
+ *   u_acc [B, L], u_res [B] fp32 uniforms in [0, 1)
+ *   accept_len [B] int32, emitted [B, L+1] int32 (kept drafts, the drawn
+ *   token, then -1)
+ * 0 <= B, 1 <= L <= 16, K in {16, 32}, K <= V < 2^31. Errors: INVALID_ARG, CUDA. */
+dflash_status dflash_verify_rejection(const int32_t *path, const int32_t *topk_ids, const float *draft_probs,
+                                      const float *target_probs, const float *u_acc, const float *u_res,
+                                      int32_t B, int32_t L, int32_t K, int64_t V, int32_t *accept_len,
+                                      int32_t *emitted, void *stream);
 
 /* Greedy verification (blog intro: the target checks the whole block in one
  * pass and keeps the right guesses; the dev.to commentary: greedy output

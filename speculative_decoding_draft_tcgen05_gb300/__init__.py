@@ -27,6 +27,7 @@ STATUS_NAMES = {0: "DFLASH_OK", 1: "DFLASH_ERR_INVALID_ARG", 2: "DFLASH_ERR_UNSU
 
 DFLASH_WALK_VITERBI = 0
 DFLASH_WALK_GREEDY = 1
+DFLASH_WALK_SAMPLE = 2
 
 KERNEL_NAMES = ("lmhead_topk", "topk_merge", "projection", "pair_walk", "select_tail")
 
@@ -40,7 +41,7 @@ class DflashError(RuntimeError):
 class dflash_select_config(ctypes.Structure):
     _fields_ = [("V", ctypes.c_int64), ("d", ctypes.c_int32), ("L", ctypes.c_int32), ("K", ctypes.c_int32),
                 ("e", ctypes.c_int32), ("max_batch", ctypes.c_int32), ("walk", ctypes.c_int32),
-                ("tie_eps", ctypes.c_float)]
+                ("tie_eps", ctypes.c_float), ("temperature", ctypes.c_float)]
 
 
 _lock = threading.Lock()
@@ -61,6 +62,8 @@ def lib() -> ctypes.CDLL:
                                              ctypes.POINTER(P)]
             L.dflash_select_run.argtypes = [P, P, P, i32, P, P, P, P, P, P, P]
             L.dflash_verify_prefix.argtypes = [P, P, i32, i32, P, P, P]
+            L.dflash_select_run_sampled.argtypes = [P, P, P, i32, P, P, P, P, P, P, P, P, P]
+            L.dflash_verify_rejection.argtypes = [P, P, P, P, P, P, i32, i32, i32, i64, P, P, P]
             L.dflash_select_step_host.argtypes = [P, P, P, P, i32, P, P, P, P]
             L.dflash_select_sync_status.argtypes = [P, P]
             L.dflash_select_profile.argtypes = [P, i32]
@@ -72,7 +75,8 @@ def lib() -> ctypes.CDLL:
             L.dflash_last_error.restype = ctypes.c_char_p
             for f in ("dflash_select_init", "dflash_select_run", "dflash_verify_prefix", "dflash_select_step_host",
                       "dflash_select_sync_status", "dflash_select_profile", "dflash_select_profile_read",
-                      "dflash_select_destroy", "dflash_lmhead_topk_noalloc"):
+                      "dflash_select_destroy", "dflash_lmhead_topk_noalloc", "dflash_select_run_sampled",
+                      "dflash_verify_rejection"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -110,12 +114,12 @@ def _stream(stream):
 
 
 def dflash_select_init(W, E, W_A, W_B, W_H, *, L: int, K: int, max_batch: int, walk: int = DFLASH_WALK_VITERBI,
-                       tie_eps: float = 1e-3, stream=None):
+                       tie_eps: float = 1e-3, temperature: float = 1.0, stream=None):
     """Creates a selector handle over device bf16 weights W [V, d], E [V, d], W_A/W_B/W_H [256, d]."""
     import torch
     V, d = W.shape
     cfg = dflash_select_config(V=V, d=d, L=L, K=K, e=W_A.shape[0], max_batch=max_batch, walk=walk,
-                               tie_eps=tie_eps)
+                               tie_eps=tie_eps, temperature=temperature)
     h = ctypes.c_void_p()
     _check(lib().dflash_select_init(ctypes.byref(cfg), _ptr(W, torch.bfloat16, "W"), _ptr(E, torch.bfloat16, "E"),
                                     _ptr(W_A, torch.bfloat16, "W_A"), _ptr(W_B, torch.bfloat16, "W_B"),
@@ -135,6 +139,38 @@ def dflash_select_run(handle, hidden, anchor, *, path, topk_ids=None, topk_vals=
                                    _ptr(pair_scores, torch.float32, "pair_scores"), _ptr(path, torch.int32, "path"),
                                    _ptr(path_score, torch.float32, "path_score"),
                                    _ptr(tie_flags, torch.uint8, "tie_flags"), _stream(stream)), "dflash_select_run")
+
+
+def dflash_select_run_sampled(handle, hidden, anchor, u_walk, *, path, draft_probs, topk_ids=None, topk_vals=None,
+                              pair_scores=None, path_score=None, tie_flags=None, stream=None):
+    """The selector with the sampling walk: u_walk [B, L] fp32 uniforms in, draft_probs [B, L, K] out."""
+    import torch
+    B = anchor.shape[0]
+    _check(lib().dflash_select_run_sampled(handle, _ptr(hidden, torch.bfloat16, "hidden"),
+                                           _ptr(anchor, torch.int32, "anchor"), B, _ptr(u_walk, torch.float32, "u_walk"),
+                                           _ptr(topk_ids, torch.int32, "topk_ids"),
+                                           _ptr(topk_vals, torch.float32, "topk_vals"),
+                                           _ptr(pair_scores, torch.float32, "pair_scores"),
+                                           _ptr(path, torch.int32, "path"), _ptr(draft_probs, torch.float32, "draft_probs"),
+                                           _ptr(path_score, torch.float32, "path_score"),
+                                           _ptr(tie_flags, torch.uint8, "tie_flags"), _stream(stream)),
+           "dflash_select_run_sampled")
+
+
+def dflash_verify_rejection(path, topk_ids, draft_probs, target_probs, u_acc, u_res, accept_len, emitted, stream=None):
+    """Rejection-sampling verification: path [B, L], topk_ids / draft_probs [B, L, K], target_probs [B, L+1, V],
+    u_acc [B, L], u_res [B] (device) into accept_len [B] and emitted [B, L+1]."""
+    import torch
+    B, L = path.shape
+    K = topk_ids.shape[2]
+    V = target_probs.shape[2]
+    _check(lib().dflash_verify_rejection(_ptr(path, torch.int32, "path"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                         _ptr(draft_probs, torch.float32, "draft_probs"),
+                                         _ptr(target_probs, torch.float32, "target_probs"),
+                                         _ptr(u_acc, torch.float32, "u_acc"), _ptr(u_res, torch.float32, "u_res"), B, L,
+                                         K, V, _ptr(accept_len, torch.int32, "accept_len"),
+                                         _ptr(emitted, torch.int32, "emitted"), _stream(stream)),
+           "dflash_verify_rejection")
 
 
 def dflash_verify_prefix(path, target, accept_len, emitted=None, stream=None):
@@ -242,11 +278,13 @@ def dflash_select_destroy(handle):
 class Selector:
     """Owns a handle and the output tensors of one batch size (convenience only)."""
 
-    def __init__(self, W, E, W_A, W_B, W_H, *, L, K, max_batch, walk=DFLASH_WALK_VITERBI, tie_eps=1e-3):
+    def __init__(self, W, E, W_A, W_B, W_H, *, L, K, max_batch, walk=DFLASH_WALK_VITERBI, tie_eps=1e-3,
+                 temperature=1.0):
         import torch
         self.L, self.K, self.max_batch = L, K, max_batch
         self.device = W.device
-        self.h = dflash_select_init(W, E, W_A, W_B, W_H, L=L, K=K, max_batch=max_batch, walk=walk, tie_eps=tie_eps)
+        self.h = dflash_select_init(W, E, W_A, W_B, W_H, L=L, K=K, max_batch=max_batch, walk=walk, tie_eps=tie_eps,
+                                    temperature=temperature)
         self._torch = torch
 
     def outputs(self, B, full=True):

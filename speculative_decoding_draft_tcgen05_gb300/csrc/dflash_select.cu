@@ -207,8 +207,10 @@ static dflash_status check_config(const dflash_select_config *c)
     if (c->e != dfl::kEmbed) return fail(DFLASH_ERR_UNSUPPORTED, "e must be 256 (got %d)", c->e);
     if (c->max_batch < 1 || static_cast<int64_t>(c->max_batch) * c->L > 8192)
         return fail(DFLASH_ERR_UNSUPPORTED, "max_batch must be >= 1 with max_batch * L <= 8192");
-    if (c->walk != DFLASH_WALK_VITERBI && c->walk != DFLASH_WALK_GREEDY)
-        return fail(DFLASH_ERR_INVALID_ARG, "walk must be DFLASH_WALK_VITERBI or DFLASH_WALK_GREEDY");
+    if (c->walk != DFLASH_WALK_VITERBI && c->walk != DFLASH_WALK_GREEDY && c->walk != DFLASH_WALK_SAMPLE)
+        return fail(DFLASH_ERR_INVALID_ARG, "walk must be DFLASH_WALK_VITERBI, _GREEDY or _SAMPLE");
+    if (c->walk == DFLASH_WALK_SAMPLE && (!(c->temperature > 0.0f) || !std::isfinite(c->temperature)))
+        return fail(DFLASH_ERR_INVALID_ARG, "the sampling walk needs a finite temperature > 0");
     if (!(c->tie_eps >= 0.0f) || !std::isfinite(c->tie_eps))
         return fail(DFLASH_ERR_INVALID_ARG, "tie_eps must be finite and >= 0");
     return ok();
@@ -354,9 +356,10 @@ static void prof_end(dflash_select_ctx *c, int slot, int kid, cudaStream_t s)
     c->prof_rec[c->prof_runs].n = slot + 1;
 }
 
-dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,
-                                int32_t *topk_ids, float *topk_vals, float *pair_scores, int32_t *path,
-                                float *path_score, uint8_t *tie_flags, void *stream)
+static dflash_status run_impl(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,
+                              const float *u_walk, int32_t *topk_ids, float *topk_vals, float *pair_scores,
+                              int32_t *path, float *draft_probs, float *path_score, uint8_t *tie_flags,
+                              void *stream)
 {
     if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
     dflash_select_ctx *c = h;
@@ -426,6 +429,9 @@ dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, cons
         tp.cs = pl.tail_cs;
         tp.walk = c->cfg.walk;
         tp.tie_eps = c->cfg.tie_eps;
+        tp.u_walk = u_walk;
+        tp.q_out = draft_probs;
+        tp.temperature = c->cfg.temperature;
         prof_begin(c, 1, s);
         CUDA_TRY(dfl::launch_select_tail(tp, c->cfg.K, pl.tail_S, pl.tail_smem, s));
         prof_end(c, 1, 4, s);
@@ -474,10 +480,54 @@ dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, cons
     q.R = c->R;
     q.walk = c->cfg.walk;
     q.tie_eps = c->cfg.tie_eps;
+    q.u_walk = u_walk;
+    q.q_out = draft_probs;
+    q.temperature = c->cfg.temperature;
     prof_begin(c, 3, s);
     CUDA_TRY(dfl::launch_pair_walk(q, s));
     prof_end(c, 3, 3, s);
     if (prof_on(c)) ++c->prof_runs;
+    return ok();
+}
+
+dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,
+                                int32_t *topk_ids, float *topk_vals, float *pair_scores, int32_t *path,
+                                float *path_score, uint8_t *tie_flags, void *stream)
+{
+    if (h && h->cfg.walk == DFLASH_WALK_SAMPLE)
+        return fail(DFLASH_ERR_INVALID_ARG, "a sampling handle runs through dflash_select_run_sampled");
+    return run_impl(h, hidden, anchor, B, nullptr, topk_ids, topk_vals, pair_scores, path, nullptr, path_score,
+                    tie_flags, stream);
+}
+
+dflash_status dflash_select_run_sampled(dflash_select_handle h, const void *hidden, const int32_t *anchor,
+                                        int32_t B, const float *u_walk, int32_t *topk_ids, float *topk_vals,
+                                        float *pair_scores, int32_t *path, float *draft_probs,
+                                        float *path_score, uint8_t *tie_flags, void *stream)
+{
+    if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+    if (h->cfg.walk != DFLASH_WALK_SAMPLE)
+        return fail(DFLASH_ERR_INVALID_ARG, "dflash_select_run_sampled needs a handle created with DFLASH_WALK_SAMPLE");
+    if (B > 0 && (!u_walk || !draft_probs))
+        return fail(DFLASH_ERR_INVALID_ARG, "u_walk and draft_probs must not be NULL");
+    return run_impl(h, hidden, anchor, B, u_walk, topk_ids, topk_vals, pair_scores, path, draft_probs, path_score,
+                    tie_flags, stream);
+}
+
+dflash_status dflash_verify_rejection(const int32_t *path, const int32_t *topk_ids, const float *draft_probs,
+                                      const float *target_probs, const float *u_acc, const float *u_res, int32_t B,
+                                      int32_t L, int32_t K, int64_t V, int32_t *accept_len, int32_t *emitted,
+                                      void *stream)
+{
+    if (B < 0) return fail(DFLASH_ERR_INVALID_ARG, "B must be >= 0 (got %d)", B);
+    if (L < 1 || L > 16) return fail(DFLASH_ERR_INVALID_ARG, "L must be in [1, 16] (got %d)", L);
+    if (K != 16 && K != 32) return fail(DFLASH_ERR_INVALID_ARG, "K must be 16 or 32 (got %d)", K);
+    if (V < K || V >= (int64_t(1) << 31)) return fail(DFLASH_ERR_INVALID_ARG, "V must satisfy K <= V < 2^31");
+    if (B == 0) return ok();
+    if (!path || !topk_ids || !draft_probs || !target_probs || !u_acc || !u_res || !accept_len || !emitted)
+        return fail(DFLASH_ERR_INVALID_ARG, "NULL argument");
+    CUDA_TRY(dfl::launch_verify_rejection(path, topk_ids, draft_probs, target_probs, u_acc, u_res, B, L, K, V,
+                                          accept_len, emitted, static_cast<cudaStream_t>(stream)));
     return ok();
 }
 

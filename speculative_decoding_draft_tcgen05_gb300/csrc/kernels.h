@@ -119,6 +119,9 @@ struct PairParams {
     uint8_t *tie_flags;   // optional [B, L]
     int B, L, K, R, walk;
     float tie_eps;
+    const float *u_walk;  // [B, L] uniforms (sampling walk)
+    float *q_out;         // [B, L, K] draft distributions (sampling walk)
+    float temperature;
 };
 cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s);
 
@@ -144,6 +147,9 @@ struct TailParams {
     int64_t V;
     int d, L, G, N, cs, walk;
     float tie_eps;
+    const float *u_walk;  // [B, L] uniforms (sampling walk)
+    float *q_out;         // [B, L, K] draft distributions (sampling walk)
+    float temperature;
 };
 int tail_cluster_size(int d);
 int tail_stages(int K, int G, int cs, int smem_optin);
@@ -154,5 +160,8 @@ cudaError_t launch_select_tail(const TailParams &p, int K, int S, size_t smem, c
 // ---- greedy accept check ----
 cudaError_t launch_verify(const int32_t *path, const int32_t *target, int B, int L, int32_t *accept,
                           int32_t *emitted, cudaStream_t s);
+cudaError_t launch_verify_rejection(const int32_t *path, const int32_t *ids, const float *q, const float *p,
+                                    const float *u_acc, const float *u_res, int B, int L, int K, int64_t V,
+                                    int32_t *accept, int32_t *emitted, cudaStream_t s);
 
 }  // namespace dfl

@@ -315,7 +315,9 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
     walk_sequence<K>(p.P + static_cast<size_t>(b) * L * K * K, p.ids + static_cast<size_t>(b) * L * K, L, p.walk,
                      p.tie_eps, pw_smem, ws, p.path + static_cast<size_t>(b) * L,
                      p.path_score ? p.path_score + b : nullptr,
-                     p.tie_flags ? p.tie_flags + static_cast<size_t>(b) * L : nullptr);
+                     p.tie_flags ? p.tie_flags + static_cast<size_t>(b) * L : nullptr,
+                     SampleArgs{p.u_walk ? p.u_walk + static_cast<size_t>(b) * L : nullptr,
+                                p.q_out ? p.q_out + static_cast<size_t>(b) * L * K : nullptr, p.temperature});
 }
 
 }  // namespace

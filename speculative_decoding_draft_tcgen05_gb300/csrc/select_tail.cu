@@ -415,7 +415,9 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
     walk_sequence<K>(p.P + static_cast<size_t>(b) * L * K * K, p.ids + static_cast<size_t>(b) * L * K, L, p.walk,
                      p.tie_eps, reinterpret_cast<float *>(gbase), ws, p.path + static_cast<size_t>(b) * L,
                      p.path_score ? p.path_score + b : nullptr,
-                     p.tie_flags ? p.tie_flags + static_cast<size_t>(b) * L : nullptr);
+                     p.tie_flags ? p.tie_flags + static_cast<size_t>(b) * L : nullptr,
+                     SampleArgs{p.u_walk ? p.u_walk + static_cast<size_t>(b) * L : nullptr,
+                                p.q_out ? p.q_out + static_cast<size_t>(b) * L * K : nullptr, p.temperature});
 }
 
 template <int K, int S>

@@ -2,11 +2,16 @@
 // Drafting Parallel", section "A Lightweight Path Selector": the only
 // sequential work is the final walk, starting from the last verified token).
 //
+// Walks (walk = 0, 1, 2):
 // Max-sum (Viterbi) walk: delta_0(j) = S_0(x0, j);
 // delta_t(j) = max_i delta_{t-1}(i) + S_t(i, j), the smallest rank i winning
 // ties; the path ends at the best final rank (smallest on ties) and is read
 // back through the back-pointers. Greedy walk: from x0, the best successor at
-// every step (smallest rank on ties). One warp, lane j = candidate rank j.
+// every step (smallest rank on ties). Sampling walk (the pages: "sampling
+// draws from the same scores"): at every step the next rank is drawn from
+// softmax(S_t(prev, .) / T) over the K candidates by inverting its CDF in rank
+// order with a given uniform u_t; the distribution is written out for the
+// rejection-sampling verifier. One warp, lane j = candidate rank j.
 #pragma once
 
 #include "common.cuh"
@@ -21,16 +26,24 @@ struct WalkSmem {
     uint8_t flags[16];
 };
 
+struct SampleArgs {
+    const float *u;  // [L] uniforms of the sequence (walk 2)
+    float *q_out;    // [L, K] drawn-from distributions (walk 2)
+    float temperature;
+};
+
 // Called by every thread of a 256-thread CTA, uniformly. Stages the L tables
 // P_seq [L, K, K] (written by other CTAs of this or an earlier kernel; read
 // around L1) into shared memory Pb, walks them with warp 0 and writes the
 // path tokens ids_seq[t * K + rank_t], the path score and the tie flags
-// (bit 0: the choice at t had a margin below tie_eps; bit 1 at t = L-1: the
-// final choice did).
+// (bit 0: the choice at t had a margin below tie_eps -- for the sampling walk,
+// the uniform lay within tie_eps of a CDF boundary; bit 1 at t = L-1: the
+// final choice of the max-sum walk did).
+
 template <int K>
 __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t *ids_seq, int L, int walk,
                                               float tie_eps, float *Pb, WalkSmem<K> &ws, int32_t *path_out,
-                                              float *score_out, uint8_t *flags_out)
+                                              float *score_out, uint8_t *flags_out, SampleArgs sa = {})
 {
     const int tid = threadIdx.x;
     {
@@ -108,6 +121,34 @@ __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t 
                 ws.flags[s] = f;
             }
         }
+    } else if (walk == 2) {
+        int prev = 0;
+        float total = 0.f;
+        for (int s = 0; s < L; ++s) {
+            const float v = active ? Pb[(s * K + prev) * K + lane] : -INFINITY;
+            float m = v;
+            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+            const float e = active ? expf((v - m) / sa.temperature) : 0.f;
+            float c = e;  // inclusive running sum in rank order
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xFFFFFFFFu, c, off);
+                if (lane >= off) c += y;
+            }
+            const float Z = __shfl_sync(0xFFFFFFFFu, c, 31);
+            const float target = __ldg(sa.u + s) * Z;
+            const unsigned above = __ballot_sync(0xFFFFFFFFu, active && c > target);
+            const int chosen = above ? __ffs(above) - 1 : K - 1;
+            float dist = (lane < K - 1) ? fabsf(c - target) / Z : INFINITY;
+            for (int off = 16; off > 0; off >>= 1) dist = fminf(dist, __shfl_xor_sync(0xFFFFFFFFu, dist, off));
+            if (sa.q_out && active) sa.q_out[s * K + lane] = e / Z;
+            if (lane == 0) {
+                ws.ranks[s] = chosen;
+                ws.flags[s] = (dist < tie_eps) ? 1 : 0;
+            }
+            total += __shfl_sync(0xFFFFFFFFu, v, chosen);
+            prev = chosen;
+        }
+        score = total;
     } else {
         int prev = 0;
         float total = 0.f;

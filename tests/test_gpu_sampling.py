@@ -1,0 +1,205 @@
+"""GPU parity of the sampling walk and the rejection-sampling verifier against
+the CPU oracle (uniform random numbers are inputs to both sides).
+
+Decisions taken by comparing a uniform with a cumulative probability are
+compared exactly, except where the oracle's own distance between the uniform
+and the decision boundary is below SAMPLE_EPS (reported, not failed), and
+where a top-K boundary is a near-tie (the candidate sets may then differ)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import parity
+from speculative_decoding_draft_tcgen05_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+SAMPLE_EPS = 1e-4
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from speculative_decoding_draft_tcgen05_gb300 import build
+    build.build()
+    import speculative_decoding_draft_tcgen05_gb300 as p
+    p.lib()
+    return p
+
+
+def _gpu_sampled(pkg, inp, hidden, anchor, u_walk, T):
+    w = inp.wl
+    B = anchor.shape[0]
+    d = parity.to_device(inp, "cuda")
+    with pkg.Selector(d["W"], d["E"], d["W_A"], d["W_B"], d["W_H"], L=w.L, K=w.K, max_batch=B,
+                      walk=pkg.DFLASH_WALK_SAMPLE, temperature=T) as sel:
+        out = sel.outputs(B)
+        out["draft_probs"] = torch.empty(B, w.L, w.K, dtype=torch.float32, device="cuda")
+        pkg.dflash_select_run_sampled(sel.h, hidden.cuda(), anchor.cuda(), torch.from_numpy(u_walk).cuda(), **out)
+        pkg.dflash_select_sync_status(sel.h)
+        torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def _target_probs(rng, q_rows, ids_rows, V, L):
+    """p_t = half the draft distribution on its candidates + half a random
+    distribution over the vocabulary; p_L random. fp32, as the GPU reads it."""
+    p = np.empty((L + 1, V), np.float64)
+    for t in range(L + 1):
+        r = rng.gamma(1.0, size=V)
+        p[t] = 0.5 * r / r.sum() if t < L else r / r.sum()
+        if t < L:
+            p[t, ids_rows[t]] += 0.5 * q_rows[t]
+    return p.astype(np.float32)
+
+
+def _check_walk(inp, gpu, seqs_hidden_idx, u_walk, T):
+    """Per replica b (hidden of sequence seqs_hidden_idx[b]): the GPU's sampled
+    path and draft distribution against the oracle's."""
+    w = inp.wl
+    orc = parity.run_oracle(inp, sorted(set(seqs_hidden_idx)))
+    rep = dict(checked=0, excused=0)
+    for b, s in enumerate(seqs_hidden_idx):
+        r = orc[s]
+        ranks, q, mg = oracle.sample_walk(r["P"], T, u_walk[b].astype(np.float64))
+        tokens = r["ids"][np.arange(w.L), ranks]
+        if (r["topk_margin"] < parity.TIE_EPS).any() or (mg < SAMPLE_EPS).any():
+            rep["excused"] += 1
+            continue
+        assert gpu["path"][b].tolist() == tokens.tolist(), f"replica {b}: sampled path"
+        for t in range(w.L):
+            by_id = dict(zip(r["ids"][t].tolist(), q[t].tolist()))
+            for j, tok in enumerate(gpu["topk_ids"][b][t].tolist()):
+                assert parity.close(gpu["draft_probs"][b][t][j], by_id[tok]), f"replica {b} t {t}: draft prob"
+        rep["checked"] += 1
+    return rep, orc
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5])
+def test_sampling_walk_tiny(pkg, T):
+    inp = parity.inputs_for("tiny")
+    rng = np.random.default_rng(41)
+    reps = 16
+    idx = [b % inp.wl.B for b in range(reps)]
+    hidden = inp.hidden[idx].contiguous()
+    anchor = inp.anchor[idx].contiguous()
+    u_walk = rng.random((reps, inp.wl.L)).astype(np.float32)
+    gpu = _gpu_sampled(pkg, inp, hidden, anchor, u_walk, T)
+    rep, _ = _check_walk(inp, gpu, idx, u_walk, T)
+    print("sampling walk tiny T", T, rep)
+    assert rep["checked"] >= reps // 2
+
+
+def _verify_case(pkg, inp, orc_seq, rng, reps, T):
+    """Rejection verifier in isolation: the oracle's draft (path, candidates,
+    fp32-rounded draft distribution) and random target rows, on both sides."""
+    w = inp.wl
+    L, K, V = w.L, w.K, w.V
+    paths, ids, qs, ps, ua, ur = [], [], [], [], [], []
+    for b in range(reps):
+        r = orc_seq
+        u = rng.random(L).astype(np.float32)
+        ranks, q, _ = oracle.sample_walk(r["P"], T, u.astype(np.float64))
+        paths.append(r["ids"][np.arange(L), ranks].astype(np.int32))
+        ids.append(r["ids"].astype(np.int32))
+        qs.append(q.astype(np.float32))
+        ps.append(_target_probs(rng, q, r["ids"], V, L))
+        ua.append(rng.random(L).astype(np.float32))
+        ur.append(np.float32(rng.random()))
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(np.stack(a) if isinstance(a, list) else a)).to(dt).cuda()
+    acc = torch.empty(reps, dtype=torch.int32, device="cuda")
+    em = torch.empty(reps, L + 1, dtype=torch.int32, device="cuda")
+    pkg.dflash_verify_rejection(t(paths, torch.int32), t(ids, torch.int32), t(qs, torch.float32),
+                                t(ps, torch.float32), t(ua, torch.float32),
+                                torch.tensor(ur, dtype=torch.float32).cuda(), acc, em)
+    torch.cuda.synchronize()
+    acc, em = acc.cpu().numpy(), em.cpu().numpy()
+    checked = excused = 0
+    ns = []
+    for b in range(reps):
+        n, e, am, rm = oracle.verify_rejection(paths[b], ids[b], qs[b].astype(np.float64), ps[b].astype(np.float64),
+                                               ua[b].astype(np.float64), float(ur[b]))
+        ns.append(n)
+        if (am[:min(n + 1, L)] < SAMPLE_EPS).any() or rm < SAMPLE_EPS:
+            excused += 1
+            continue
+        assert acc[b] == n, f"replica {b}: accept length"
+        assert em[b].tolist() == e.tolist(), f"replica {b}: emitted"
+        checked += 1
+    return checked, excused, ns
+
+
+@pytest.mark.parametrize("name", ["tiny", "4b_b1"])
+def test_rejection_verifier_against_oracle(pkg, name):
+    inp = parity.inputs_for(name)
+    orc = parity.run_oracle(inp, [0])[0]
+    rng = np.random.default_rng(43)
+    checked, excused, ns = _verify_case(pkg, inp, orc, rng, reps=48, T=1.0)
+    print(name, "rejection verifier: checked", checked, "excused", excused, "accept lengths", np.bincount(ns))
+    assert checked >= 40
+    assert len(set(ns)) > 2  # both rejections at several depths and full acceptances occur
+
+
+def test_sampled_step_end_to_end_full_size(pkg):
+    """Qwen3-4B-shaped head at full size: GPU sampled walk then GPU verifier,
+    against the oracle's walk then the oracle's verifier, 8 uniform draws."""
+    inp = parity.inputs_for("4b_b1")
+    w = inp.wl
+    rng = np.random.default_rng(47)
+    reps = 8
+    idx = [0] * reps
+    hidden = inp.hidden[idx].contiguous()
+    anchor = inp.anchor[idx].contiguous()
+    u_walk = rng.random((reps, w.L)).astype(np.float32)
+    gpu = _gpu_sampled(pkg, inp, hidden, anchor, u_walk, 1.0)
+    rep, orc = _check_walk(inp, gpu, idx, u_walk, 1.0)
+    r = orc[0]
+    ps, ua, ur, onum = [], [], [], []
+    for b in range(reps):
+        ranks, q, _ = oracle.sample_walk(r["P"], 1.0, u_walk[b].astype(np.float64))
+        ps.append(_target_probs(rng, q, r["ids"], w.V, w.L))
+        ua.append(rng.random(w.L).astype(np.float32))
+        ur.append(np.float32(rng.random()))
+    acc = torch.empty(reps, dtype=torch.int32, device="cuda")
+    em = torch.empty(reps, w.L + 1, dtype=torch.int32, device="cuda")
+    pkg.dflash_verify_rejection(torch.from_numpy(gpu["path"]).cuda(), torch.from_numpy(gpu["topk_ids"]).cuda(),
+                                torch.from_numpy(gpu["draft_probs"]).cuda(), torch.from_numpy(np.stack(ps)).cuda(),
+                                torch.from_numpy(np.stack(ua)).cuda(), torch.tensor(ur, dtype=torch.float32).cuda(),
+                                acc, em)
+    torch.cuda.synchronize()
+    acc, em = acc.cpu().numpy(), em.cpu().numpy()
+    checked = 0
+    for b in range(reps):
+        ranks, q, mg = oracle.sample_walk(r["P"], 1.0, u_walk[b].astype(np.float64))
+        path = r["ids"][np.arange(w.L), ranks]
+        n, e, am, rm = oracle.verify_rejection(path, r["ids"], q, ps[b].astype(np.float64), ua[b].astype(np.float64),
+                                               float(ur[b]))
+        if (mg < SAMPLE_EPS).any() or (am[:min(n + 1, w.L)] < SAMPLE_EPS).any() or rm < SAMPLE_EPS:
+            continue
+        assert acc[b] == n and em[b].tolist() == e.tolist(), f"replica {b}"
+        checked += 1
+    print("sampled step 4b_b1:", rep, "verified", checked)
+    assert rep["checked"] >= reps // 2 and checked >= reps // 2
+
+
+def test_sampling_arguments(pkg):
+    inp = parity.inputs_for("tiny")
+    d = parity.to_device(inp, "cuda")
+    w = inp.wl
+    with pytest.raises(pkg.DflashError):
+        pkg.dflash_select_init(d["W"], d["E"], d["W_A"], d["W_B"], d["W_H"], L=w.L, K=w.K, max_batch=2,
+                               walk=pkg.DFLASH_WALK_SAMPLE, temperature=0.0)
+    with pkg.Selector(d["W"], d["E"], d["W_A"], d["W_B"], d["W_H"], L=w.L, K=w.K, max_batch=2,
+                      walk=pkg.DFLASH_WALK_SAMPLE) as sel:
+        out = sel.outputs(2)
+        with pytest.raises(pkg.DflashError) as e:  # a sampling handle needs its uniforms
+            pkg.dflash_select_run(sel.h, d["hidden"], d["anchor"], **out)
+        assert e.value.status == pkg.DFLASH_ERR_INVALID_ARG
+    with pkg.Selector(d["W"], d["E"], d["W_A"], d["W_B"], d["W_H"], L=w.L, K=w.K, max_batch=2) as sel:
+        out = sel.outputs(2)
+        q = torch.empty(2, w.L, w.K, dtype=torch.float32, device="cuda")
+        u = torch.rand(2, w.L, device="cuda")
+        with pytest.raises(pkg.DflashError):  # a max-sum handle does not sample
+            pkg.dflash_select_run_sampled(sel.h, d["hidden"], d["anchor"], u, draft_probs=q, **out)
