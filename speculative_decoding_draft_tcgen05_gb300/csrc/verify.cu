@@ -56,6 +56,10 @@ cudaError_t launch_verify(const int32_t *path, const int32_t *target, int B, int
 // One CTA of 1024 threads per sequence: lanes decide the L acceptances in
 // parallel, then each thread sums a contiguous slice of the vocabulary, a
 // block scan locates the slice holding u_res * Z, and its owner walks it.
+// The ratio and the residual's running sums are taken in double precision, so
+// each decision matches an exact computation unless the uniform lies within
+// about 1e-12 of a boundary (the CDF steps of a 150k-token vocabulary are
+// ~1e-5, as small as fp32 summation error).
 namespace dfl {
 
 namespace {
@@ -70,7 +74,7 @@ __global__ void __launch_bounds__(kRejThreads) verify_rejection_kernel(
     __shared__ int s_n;
     __shared__ int32_t s_cand[32];
     __shared__ float s_q[32];
-    __shared__ float s_warp[32];
+    __shared__ double s_warp[32];
     __shared__ int s_owner;
     __shared__ int32_t s_draw;
     pdl_trigger();
@@ -89,9 +93,9 @@ __global__ void __launch_bounds__(kRejThreads) verify_rejection_kernel(
             float qx = 0.f;
             for (int j = 0; j < K; ++j)
                 if (__ldg(ib + lane * K + j) == x) qx = __ldg(qb + lane * K + j);
-            const float px = (x >= 0 && x < V) ? __ldg(prow0 + static_cast<size_t>(lane) * V + x) : 0.f;
-            const float a = (qx > 0.f) ? fminf(1.f, px / qx) : 0.f;
-            keep = __ldg(u_acc + static_cast<size_t>(b) * L + lane) < a;
+            const double px = (x >= 0 && x < V) ? __ldg(prow0 + static_cast<size_t>(lane) * V + x) : 0.0;
+            const double a = (qx > 0.f) ? fmin(1.0, px / static_cast<double>(qx)) : 0.0;
+            keep = static_cast<double>(__ldg(u_acc + static_cast<size_t>(b) * L + lane)) < a;
         }
         const unsigned rejected = ~__ballot_sync(0xFFFFFFFFu, keep) & ((L >= 32) ? 0xFFFFFFFFu : ((1u << L) - 1u));
         const int n = rejected ? __ffs(rejected) - 1 : L;
@@ -109,57 +113,48 @@ __global__ void __launch_bounds__(kRejThreads) verify_rejection_kernel(
     // this thread's slice of the vocabulary and its mass
     const int64_t chunk = (V + kRejThreads - 1) / kRejThreads;
     const int64_t y0 = tid * chunk, y1 = (y0 + chunk < V) ? y0 + chunk : V;
-    auto mass = [&](int64_t y, float py) -> float {
+    auto mass = [&](int64_t y, double py) -> double {
         if (residual)
             for (int j = 0; j < K; ++j)
-                if (s_cand[j] == y) return fmaxf(0.f, py - s_q[j]);
+                if (s_cand[j] == y) return fmax(0.0, py - static_cast<double>(s_q[j]));
         return py;
     };
-    float part = 0.f;
-    for (int64_t y = y0; y < y1; ++y) part += __ldg(row + y);
-    if (residual)
-        for (int j = 0; j < K; ++j) {
-            const int64_t c = s_cand[j];
-            if (c >= y0 && c < y1) {
-                const float pc = __ldg(row + c);
-                part += fmaxf(0.f, pc - s_q[j]) - pc;
-            }
-        }
-    part = fmaxf(part, 0.f);
+    double part = 0.0;
+    for (int64_t y = y0; y < y1; ++y) part += mass(y, __ldg(row + y));
     // block-wide exclusive scan of the slice masses
-    float incl = part;
+    double incl = part;
     for (int off = 1; off < 32; off <<= 1) {
-        const float v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        const double v = __shfl_up_sync(0xFFFFFFFFu, incl, off);
         if (lane >= off) incl += v;
     }
     if (lane == 31) s_warp[warp] = incl;
     if (tid == 0) s_owner = -1;
     __syncthreads();
     if (warp == 0) {
-        float w = s_warp[lane];
+        double w = s_warp[lane];
         for (int off = 1; off < 32; off <<= 1) {
-            const float v = __shfl_up_sync(0xFFFFFFFFu, w, off);
+            const double v = __shfl_up_sync(0xFFFFFFFFu, w, off);
             if (lane >= off) w += v;
         }
         s_warp[lane] = w;  // inclusive over warps
     }
     __syncthreads();
-    const float Z = s_warp[31];
-    const float excl = incl - part + (warp > 0 ? s_warp[warp - 1] : 0.f);
-    const float target = __ldg(u_res + b) * Z;
-    if (part > 0.f && target >= excl && target < excl + part) s_owner = tid;
+    const double Z = s_warp[31];
+    const double excl = incl - part + (warp > 0 ? s_warp[warp - 1] : 0.0);
+    const double target = static_cast<double>(__ldg(u_res + b)) * Z;
+    if (part > 0.0 && target >= excl && target < excl + part) s_owner = tid;
     __syncthreads();
     if (s_owner < 0) {  // target at the very top (rounding): the last slice with mass owns it
-        const unsigned has = __ballot_sync(0xFFFFFFFFu, part > 0.f);
+        const unsigned has = __ballot_sync(0xFFFFFFFFu, part > 0.0);
         if (lane == 0 && has) atomicMax(&s_owner, warp * 32 + 31 - __clz(has));
         __syncthreads();
     }
     if (tid == s_owner) {
-        float c = excl;
+        double c = excl;
         int32_t draw = -1, last = -1;
         for (int64_t y = y0; y < y1; ++y) {
-            const float m = mass(y, __ldg(row + y));
-            if (m <= 0.f) continue;
+            const double m = mass(y, __ldg(row + y));
+            if (m <= 0.0) continue;
             last = static_cast<int32_t>(y);
             c += m;
             if (c > target) {

@@ -15,7 +15,9 @@ from speculative_decoding_draft_tcgen05_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-SAMPLE_EPS = 1e-4
+SAMPLE_EPS = 1e-4  # the walk: GPU and oracle tables differ by ~1e-6
+EXACT_EPS = 1e-9   # the verifier on identical inputs (double precision on both sides)
+DRAW_EPS = 1e-5    # the final draw when the draft probabilities come from the GPU
 
 
 @pytest.fixture(scope="module")
@@ -122,7 +124,7 @@ def _verify_case(pkg, inp, orc_seq, rng, reps, T):
         n, e, am, rm = oracle.verify_rejection(paths[b], ids[b], qs[b].astype(np.float64), ps[b].astype(np.float64),
                                                ua[b].astype(np.float64), float(ur[b]))
         ns.append(n)
-        if (am[:min(n + 1, L)] < SAMPLE_EPS).any() or rm < SAMPLE_EPS:
+        if (am[:min(n + 1, L)] < EXACT_EPS).any() or rm < EXACT_EPS:
             excused += 1
             continue
         assert acc[b] == n, f"replica {b}: accept length"
@@ -138,7 +140,7 @@ def test_rejection_verifier_against_oracle(pkg, name):
     rng = np.random.default_rng(43)
     checked, excused, ns = _verify_case(pkg, inp, orc, rng, reps=48, T=1.0)
     print(name, "rejection verifier: checked", checked, "excused", excused, "accept lengths", np.bincount(ns))
-    assert checked >= 40
+    assert checked >= 46
     assert len(set(ns)) > 2  # both rejections at several depths and full acceptances occur
 
 
@@ -170,17 +172,22 @@ def test_sampled_step_end_to_end_full_size(pkg):
                                 acc, em)
     torch.cuda.synchronize()
     acc, em = acc.cpu().numpy(), em.cpu().numpy()
-    checked = 0
+    checked = draws = 0
     for b in range(reps):
         ranks, q, mg = oracle.sample_walk(r["P"], 1.0, u_walk[b].astype(np.float64))
         path = r["ids"][np.arange(w.L), ranks]
         n, e, am, rm = oracle.verify_rejection(path, r["ids"], q, ps[b].astype(np.float64), ua[b].astype(np.float64),
                                                float(ur[b]))
-        if (mg < SAMPLE_EPS).any() or (am[:min(n + 1, w.L)] < SAMPLE_EPS).any() or rm < SAMPLE_EPS:
+        if (mg < SAMPLE_EPS).any() or (am[:min(n + 1, w.L)] < SAMPLE_EPS).any():
             continue
-        assert acc[b] == n and em[b].tolist() == e.tolist(), f"replica {b}"
+        assert acc[b] == n and em[b][:n].tolist() == e[:n].tolist(), f"replica {b}: kept drafts"
         checked += 1
-    print("sampled step 4b_b1:", rep, "verified", checked)
+        # the drawn token depends on the draft probabilities, which differ by
+        # ~1e-7 between the GPU's fp32 softmax and the oracle's fp64 one
+        if rm >= DRAW_EPS:
+            assert em[b][n] == e[n], f"replica {b}: drawn token"
+            draws += 1
+    print("sampled step 4b_b1:", rep, "verified", checked, "draws compared", draws)
     assert rep["checked"] >= reps // 2 and checked >= reps // 2
 
 
