@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="max-sum", choices=["max-sum", "sample"],
+                    help="max-sum walk + greedy accept check (default), or sampling walk + rejection sampling")
     return ap.parse_args()
 
 
@@ -272,6 +274,50 @@ def run_reference(args):
     return 0
 
 
+def lmhead_geometry(w, sms):
+    """Positions, position-tile width, tiles and CTAs per tile of the lm_head
+    kernel (the library's own rule)."""
+    N = w.B * w.L
+    if N <= 256:
+        n_tiles = (N + 127) // 128
+        NT = ((-(-N // n_tiles)) + 15) // 16 * 16
+    else:
+        NT, n_tiles = 256, (N + 255) // 256
+    m_total = math.ceil(w.V / 128) + 2
+    G = max(1, min(m_total, sms // n_tiles))
+    return N, NT, n_tiles, G
+
+
+def finish_sample_line(args, w, world, rank, ms, prof, clk, sel, launches, extra_bytes, sms):
+    """The JSON line of the sampling step (sampling walk + rejection sampling)."""
+    N, NT, n_tiles, G = lmhead_geometry(w, sms)
+    k1_bytes, all_bytes = algorithmic_bytes(w, G, N)
+    all_bytes += extra_bytes
+    k1_ms, k1_n = prof["lmhead_topk"]
+    k1_avg_s = k1_ms / max(1, k1_n) / 1e3
+    peak, peak_kind = hbm_peak()
+    step_s = ms / 1e3 / args.steps
+    step_launches = launches * args.steps
+    sel.close()
+    if rank == 0:
+        line = {"metric": METRIC, "value": whole_job_value(w.B, world, args.steps, ms), "unit": UNIT,
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": w.label, "mode": "sampling walk (T=1) + rejection-sampling verification",
+                           "B": w.B, "L": w.L, "K": w.K, "V": w.V, "d": w.d},
+                "hbm_gbs_step": all_bytes / step_s / 1e9, "hbm_frac_step": all_bytes / step_s / 1e9 / peak,
+                "roofline": {"bound": "hbm", "kernel": "lmhead_topk", "achieved": k1_bytes / k1_avg_s / 1e9,
+                             "peak": peak, "unit": "GB/s", "frac": k1_bytes / k1_avg_s / 1e9 / peak,
+                             "algorithmic_bytes_per_launch": k1_bytes, "avg_launch_us": k1_avg_s * 1e6,
+                             "traffic": committed_traffic(args.workload)},
+                "kernels_avg_us": {k: v[0] / v[1] * 1e3 for k, v in prof.items() if v[1]},
+                "clocks": clk, "gpu_launches": step_launches,
+                "e2e": None, "e2e_note": "the host-buffer entry point covers the max-sum step only"}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ours(args):
     import torch
     import speculative_decoding_draft_tcgen05_gb300 as pkg
@@ -293,20 +339,38 @@ def run_ours(args):
     hidden = inp.hidden.to(dev)
     anchor = inp.anchor.to(dev)
     stream = torch.cuda.Stream(dev)
-    sel = pkg.Selector(W, E, WA, WB, WH, L=w.L, K=w.K, max_batch=w.B)
+    sample = args.mode == "sample"
+    sel = pkg.Selector(W, E, WA, WB, WH, L=w.L, K=w.K, max_batch=w.B,
+                       walk=pkg.DFLASH_WALK_SAMPLE if sample else pkg.DFLASH_WALK_VITERBI, temperature=1.0)
     out = sel.outputs(w.B, full=False)
     accept = torch.empty(w.B, dtype=torch.int32, device=dev)
     emitted = torch.empty(w.B, w.L + 1, dtype=torch.int32, device=dev)
-
-    # target tokens: planted on the selector's own path from an untimed run
-    # (they only set how long the accepted prefixes are)
-    with torch.cuda.stream(stream):
-        pkg.dflash_select_run(sel.h, hidden, anchor, stream=stream, **out)
-    stream.synchronize()
-    target = wl.plant_targets(out["path"].cpu(), inp.target_rand, inp.n0, w.V).to(dev)
-
-    step = pkg.bind_step(sel.h, hidden, anchor, target=target, accept_len=accept, emitted=emitted, stream=stream,
-                         **out)
+    sample_bytes = 0
+    if sample:
+        # seeded uniforms and target distributions (random rows over the vocabulary)
+        g = torch.Generator().manual_seed(w.seed + 1000)
+        u_walk = torch.rand(w.B, w.L, generator=g).to(dev)
+        u_acc = torch.rand(w.B, w.L, generator=g).to(dev)
+        u_res = torch.rand(w.B, generator=g).to(dev)
+        tprob = torch.rand(w.B, w.L + 1, w.V, generator=g)
+        tprob = (tprob / tprob.sum(-1, keepdim=True)).to(dev)
+        topk_ids = torch.empty(w.B, w.L, w.K, dtype=torch.int32, device=dev)
+        draft = torch.empty(w.B, w.L, w.K, dtype=torch.float32, device=dev)
+        step = pkg.bind_sampled_step(sel.h, hidden, anchor, u_walk, topk_ids, out["path"], draft, tprob, u_acc,
+                                     u_res, accept, emitted, stream=stream)
+        # the verifier reads one whole target row per sequence (the residual or
+        # bonus distribution), the target probability of each draft, the draft
+        # distributions (written by the walk, read back) and the uniforms
+        sample_bytes = (w.B * w.V * 4 + w.B * w.L * 4 + w.B * w.L * w.K * 4 * 2 + w.B * (2 * w.L + 1) * 4)
+    else:
+        # target tokens: planted on the selector's own path from an untimed run
+        # (they only set how long the accepted prefixes are)
+        with torch.cuda.stream(stream):
+            pkg.dflash_select_run(sel.h, hidden, anchor, stream=stream, **out)
+        stream.synchronize()
+        target = wl.plant_targets(out["path"].cpu(), inp.target_rand, inp.n0, w.V).to(dev)
+        step = pkg.bind_step(sel.h, hidden, anchor, target=target, accept_len=accept, emitted=emitted,
+                             stream=stream, **out)
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -346,6 +410,13 @@ def run_ours(args):
     ms = max_over_ranks(ms, world)
 
     # end to end through the host-buffer entry point: pinned inputs in, results out, every step
+    if sample:  # the host-buffer entry point covers the max-sum step only
+        rc = finish_sample_line(args, w, world, rank, ms, prof, clk, sel,
+                                launches=pkg.dflash_select_launches_per_run(sel.h, w.B) + 1, extra_bytes=sample_bytes,
+                                sms=torch.cuda.get_device_properties(dev).multi_processor_count)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return rc
     hid_h = inp.hidden.pin_memory()
     anc_h = inp.anchor.pin_memory()
     tgt_h = target.cpu().pin_memory()
@@ -365,12 +436,8 @@ def run_ours(args):
     d2h = path_h.numel() * 4 + acc_h.numel() * 4 + em_h.numel() * 4 + 4
 
     launches_per_step = pkg.dflash_select_launches_per_run(sel.h, w.B) + 1
-    N = w.B * w.L
-    NT = ((N + 15) // 16) * 16 if N <= 256 else 256
-    n_tiles = math.ceil(N / NT)
-    m_total = math.ceil(w.V / 128) + 2
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    G = max(1, min(m_total, sms // n_tiles))
+    N, NT, n_tiles, G = lmhead_geometry(w, sms)
     k1_bytes, all_bytes = algorithmic_bytes(w, G, N)
     k1_ms, k1_n = prof["lmhead_topk"]
     k1_avg_s = k1_ms / max(1, k1_n) / 1e3

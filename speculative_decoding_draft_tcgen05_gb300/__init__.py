@@ -271,6 +271,35 @@ def dflash_lmhead_topk_noalloc(W, hidden, K, topk_ids, topk_vals=None, device_st
            "dflash_lmhead_topk_noalloc")
 
 
+def bind_sampled_step(handle, hidden, anchor, u_walk, topk_ids, path, draft_probs, target_probs, u_acc, u_res,
+                      accept_len, emitted, stream=None):
+    """Marshals one dflash_select_run_sampled + dflash_verify_rejection pair
+    once; returns a zero-argument callable that makes both calls again."""
+    import torch
+    L_ = lib()
+    B, L = path.shape
+    K = topk_ids.shape[2]
+    V = target_probs.shape[2]
+    st = _stream(stream)
+    run_args = (handle, _ptr(hidden, torch.bfloat16, "hidden"), _ptr(anchor, torch.int32, "anchor"), B,
+                _ptr(u_walk, torch.float32, "u_walk"), _ptr(topk_ids, torch.int32, "topk_ids"), None, None,
+                _ptr(path, torch.int32, "path"), _ptr(draft_probs, torch.float32, "draft_probs"), None, None, st)
+    ver_args = (_ptr(path, torch.int32, "path"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                _ptr(draft_probs, torch.float32, "draft_probs"), _ptr(target_probs, torch.float32, "target_probs"),
+                _ptr(u_acc, torch.float32, "u_acc"), _ptr(u_res, torch.float32, "u_res"), B, L, K, V,
+                _ptr(accept_len, torch.int32, "accept_len"), _ptr(emitted, torch.int32, "emitted"), st)
+    run, ver = L_.dflash_select_run_sampled, L_.dflash_verify_rejection
+
+    def step():
+        r = run(*run_args)
+        if r:
+            _check(r, "dflash_select_run_sampled")
+        r = ver(*ver_args)
+        if r:
+            _check(r, "dflash_verify_rejection")
+    return step
+
+
 def dflash_select_destroy(handle):
     _check(lib().dflash_select_destroy(handle), "dflash_select_destroy")
 
