@@ -86,3 +86,23 @@ def test_rejection_special_cases():
         p2[0] /= p2[0].sum()
         n, emitted, _, _ = oracle.verify_rejection(path, ids, q, p2, u[L:2 * L], u[2 * L])
         assert n == 0 and emitted[0] not in ids[0].tolist() and (emitted[1:] == -1).all()
+
+
+def test_hand_worked_rejection_and_draw():
+    """One draft rejected, worked by hand: p_0 = (0.1, 0.2, 0.3, 0.4), the only
+    candidate is token 2 with q = 1. Acceptance min(1, 0.3/1) = 0.3 < u = 0.5, so
+    it is rejected; the residual is (0.1, 0.2, 0, 0.4) with Z = 0.7; u_res = 0.2
+    gives the target 0.14, crossed in vocabulary order at token 1 (running sums
+    0.1, 0.3). With u_acc = 0.25 the draft is kept and the bonus comes from p_1."""
+    ids = np.array([[2]], np.int32)
+    path = np.array([2], np.int32)
+    q = np.array([[1.0]])
+    p = np.array([[0.1, 0.2, 0.3, 0.4], [0.5, 0.25, 0.125, 0.125]])
+    n, emitted, am, rm = oracle.verify_rejection(path, ids, q, p, [0.5], 0.2)
+    assert n == 0 and emitted.tolist() == [1, -1]
+    assert abs(am[0] - 0.2) < 1e-12
+    assert abs(rm - (0.14 - 0.1) / 0.7) < 1e-12  # the nearest CDF boundary is 0.1 (0.3 is farther)
+    for u_res, tok in [(0.1, 0), (0.5, 3), (0.99, 3)]:  # targets 0.07, 0.35, 0.693
+        assert oracle.verify_rejection(path, ids, q, p, [0.5], u_res)[1][0] == tok
+    n, emitted, _, _ = oracle.verify_rejection(path, ids, q, p, [0.25], 0.6)  # bonus: target 0.6 in (0.5, 0.75]
+    assert n == 1 and emitted.tolist() == [2, 1]
