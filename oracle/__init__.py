@@ -64,6 +64,7 @@ def _load():
             lib.oracle_sample_walk.argtypes = [i32, i32, P, ctypes.c_double, P, P, P, P]
             lib.oracle_verify_rejection.argtypes = [i32, i32, i64, P, P, P, P, P, ctypes.c_double, P, P, P]
             lib.oracle_verify_rejection.restype = i32
+            lib.oracle_conv2.argtypes = [i64, i64, i64, P, P, P, P, i32]
             _lib = lib
     return _lib
 
@@ -234,3 +235,15 @@ def verify_rejection(path, ids, q, p, u_acc, u_res: float):
     n = _load().oracle_verify_rejection(L, K, V, _p(path), _p(ids), _p(q), _p(p), _p(u_acc), float(u_res),
                                         _p(emitted), _p(am), _p(rm))
     return int(n), emitted, am, float(rm[0])
+
+
+def conv2(X_bits, base_bits, Wc_bits, nthreads: int = 1) -> np.ndarray:
+    """Two-tap dynamic depthwise convolution of blocks X [B, S, d] (bf16 bits)
+    with base kernels [2, d] and correction weights Wc [2 d/16, d] (bf16 bits):
+    Y [B, S, d] in fp64."""
+    X_bits, base_bits, Wc_bits = _u16(X_bits), _u16(base_bits), _u16(Wc_bits)
+    B, S, d = X_bits.shape
+    assert d % 16 == 0 and base_bits.shape == (2, d) and Wc_bits.shape == (2 * (d // 16), d)
+    Y = np.empty((B, S, d), dtype=np.float64)
+    _load().oracle_conv2(B, S, d, _p(X_bits), _p(base_bits), _p(Wc_bits), _p(Y), int(nthreads))
+    return Y

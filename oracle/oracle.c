@@ -437,3 +437,48 @@ int oracle_verify_rejection(int L, int K, int64_t V, const int32_t *path, const 
     free(r);
     return n;
 }
+
+/* ---------------------------------------------------------------------------
+ * Two-tap dynamic depthwise convolution. Blog "DFlash 2: Keep Drafting
+ * Parallel", section "A Lightweight Local Convolution": Conv_k(x)_t =
+ * k_{t,0} (.) x_t + k_{t,1} (.) x_{t-1}; each coefficient is a learned base
+ * kernel plus a small correction computed from the current hidden state, and
+ * every 16 channels share one correction; the first draft position reads the
+ * last verified token's representation, each later one its predecessor's; the
+ * convolution is block-local and stateless. Readings (listed in the design
+ * notes):
+ *   C1  a block is S rows: the last verified token's representation, then the
+ *       draft positions; row 0 has no predecessor (x_{-1} = 0);
+ *   C2  k_{t,i}[c] = base[i, c] + corr_{t,i}[c / 16], with the correction a
+ *       linear map of x_t without bias: corr_{t,i}[g] = Wc[2 g + i] . x_t
+ *       (Wc has 2 d/16 rows, the two taps of group g interleaved).
+ * ------------------------------------------------------------------------- */
+
+/* X [B, S, d], base [2, d], Wc [2 (d/16), d] as bf16 bits; Y [B, S, d]. */
+void oracle_conv2(int64_t B, int64_t S, int64_t d, const uint16_t *X, const uint16_t *base, const uint16_t *Wc,
+                  double *Y, int nthreads)
+{
+    const int64_t G = d / 16;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic, 1)
+#endif
+    for (int64_t row = 0; row < B * S; ++row) {
+        const int64_t t = row % S;
+        const uint16_t *xt = X + row * d;
+        const uint16_t *xprev = t > 0 ? xt - d : NULL;
+        double *corr = (double *)malloc((size_t)(2 * G) * sizeof(double));
+        for (int64_t r = 0; r < 2 * G; ++r) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < d; ++j) acc += bf16_to_f64(Wc[r * d + j]) * bf16_to_f64(xt[j]);
+            corr[r] = acc;
+        }
+        for (int64_t c = 0; c < d; ++c) {
+            const int64_t g = c / 16;
+            const double k0 = bf16_to_f64(base[c]) + corr[2 * g];
+            const double k1 = bf16_to_f64(base[d + c]) + corr[2 * g + 1];
+            const double prev = xprev ? bf16_to_f64(xprev[c]) : 0.0;
+            Y[row * d + c] = k0 * bf16_to_f64(xt[c]) + k1 * prev;
+        }
+        free(corr);
+    }
+}
