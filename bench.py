@@ -14,6 +14,7 @@ time is the max over ranks and rank 0 prints the line.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -45,8 +46,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", default="max-sum", choices=["max-sum", "sample"],
-                    help="max-sum walk + greedy accept check (default), or sampling walk + rejection sampling")
+    ap.add_argument("--mode", default="max-sum", choices=["max-sum", "sample", "conv"],
+                    help="max-sum walk + greedy accept check (default), sampling walk + rejection sampling, or the "
+                         "drafter's two-tap dynamic convolution over the workload's blocks")
     return ap.parse_args()
 
 
@@ -483,10 +485,110 @@ def run_ours(args):
     return 0
 
 
+CONVS_PER_FORWARD = 20  # before and after each attention and feed-forward sublayer of a five-layer drafter
+
+
+def run_conv(args):
+    """The two-tap dynamic convolution over the workload's blocks [B, L+1, d],
+    as a drafter forward runs it: twenty convolutions, each with its own
+    weights, chained (each reads the previous one's output). A step is those
+    twenty calls, launched back to back; L2 is flushed (a 256 MB write outside
+    the events) before every step, so every call reads its weights from HBM."""
+    import torch
+    import speculative_decoding_draft_tcgen05_gb300 as pkg
+    from speculative_decoding_draft_tcgen05_gb300 import build as pbuild
+    from speculative_decoding_draft_tcgen05_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    pbuild.build()
+    L_ = pkg.lib()
+    w = wl.WORKLOADS[args.workload]
+    S = w.L + 1
+    n = CONVS_PER_FORWARD
+    convs, bufs = [], []
+    for i in range(n):
+        ci = wl.make_conv_inputs(w.B, S, w.d, seed=w.seed + 2000 + i)
+        convs.append(pkg.Conv2(ci.base.to(dev), ci.Wc.to(dev)))
+        if i == 0:
+            bufs.append(ci.X.to(dev))
+        bufs.append(torch.empty(w.B, S, w.d, dtype=torch.bfloat16, device=dev))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    st = ctypes.c_void_p(stream.cuda_stream)
+    calls = [(convs[i].h, ctypes.c_void_p(bufs[i].data_ptr()), w.B, S, ctypes.c_void_p(bufs[i + 1].data_ptr()), st)
+             for i in range(n)]
+
+    def step():
+        for a in calls:
+            L_.dflash_conv2_run(*a)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    for c in convs:
+        pkg.dflash_conv2_sync_status(c.h, stream=stream)
+    steps = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else (gpu_id or local)
+    clocks = ClockSampler(gpu_id)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    for c in convs:
+        pkg.dflash_conv2_sync_status(c.h, stream=stream)
+        c.close()
+    step_ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    step_ms = max_over_ranks(step_ms, world)
+    call_ms = step_ms / n
+    P = w.B * S
+    nbytes = (w.d // 8) * w.d * 2 + 2 * w.d * 2 + 2 * P * w.d * 2  # Wc, base, X read once, Y written
+    flops = 2.0 * P * (w.d // 8) * w.d + 4.0 * P * w.d
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / (call_ms / 1e3) / 1e9
+    if rank == 0:
+        line = {"metric": METRIC, "value": w.B * world / (step_ms / 1e3), "unit": UNIT, "n_gpus": world,
+                "steps": steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.label, "mode": "two-tap dynamic convolution: %d chained calls with their own "
+                           "weights (one drafter forward)" % n, "B": w.B, "S": S, "d": w.d,
+                           "l2": "flushed before every step (256 MB write outside the events)"},
+                "call_us": call_ms * 1e3,
+                "roofline": {"bound": "hbm", "kernel": "conv2", "achieved": achieved, "peak": peak,
+                             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                             else "fallback 6.8 TB/s", "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                             "algorithmic_bytes_per_launch": nbytes, "flops_per_launch": flops,
+                             "avg_launch_us": call_ms * 1e3},
+                "clocks": clk, "gpu_launches": steps * n, "e2e": None,
+                "e2e_note": "no host-buffer entry point for the convolution"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "conv":
+        return run_conv(args)
     return run_ours(args)
 
 

@@ -1,7 +1,8 @@
 """DFlash 2 path selector on one GB300 GPU: Python binding of libdflash_select.
 
 The functions below have the names of the C entry points declared in
-``include/dflash_select.h`` and only marshal arguments: every step of the
+``include/dflash_select.h`` and ``include/dflash_conv2.h`` and only marshal
+arguments: every step of the
 selector runs in the library's CUDA kernels. PyTorch supplies device memory
 and streams. If the library has not been built the calls raise; there is no
 fallback.
@@ -72,11 +73,16 @@ def lib() -> ctypes.CDLL:
             L.dflash_select_launches_per_run.restype = i32
             L.dflash_select_destroy.argtypes = [P]
             L.dflash_lmhead_topk_noalloc.argtypes = [P, i64, i32, P, i32, i32, P, P, P, P]
+            L.dflash_conv2_init.argtypes = [P, P, i32, ctypes.POINTER(P)]
+            L.dflash_conv2_run.argtypes = [P, P, i32, i32, P, P]
+            L.dflash_conv2_sync_status.argtypes = [P, P]
+            L.dflash_conv2_destroy.argtypes = [P]
             L.dflash_last_error.restype = ctypes.c_char_p
             for f in ("dflash_select_init", "dflash_select_run", "dflash_verify_prefix", "dflash_select_step_host",
                       "dflash_select_sync_status", "dflash_select_profile", "dflash_select_profile_read",
                       "dflash_select_destroy", "dflash_lmhead_topk_noalloc", "dflash_select_run_sampled",
-                      "dflash_verify_rejection"):
+                      "dflash_verify_rejection", "dflash_conv2_init", "dflash_conv2_run", "dflash_conv2_sync_status",
+                      "dflash_conv2_destroy"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -314,6 +320,7 @@ class Selector:
         self.device = W.device
         self.h = dflash_select_init(W, E, W_A, W_B, W_H, L=L, K=K, max_batch=max_batch, walk=walk, tie_eps=tie_eps,
                                     temperature=temperature)
+        self._weights = (W, E, W_A, W_B, W_H)  # the handle borrows them: keep them alive with it
         self._torch = torch
 
     def outputs(self, B, full=True):
@@ -338,6 +345,64 @@ class Selector:
         if self.h is not None:
             dflash_select_destroy(self.h)
             self.h = None
+            self._weights = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def dflash_conv2_init(base, Wc):
+    """Handle of one two-tap dynamic convolution: base [2, d] and Wc [d/8, d] bf16 device weights (borrowed)."""
+    import torch
+    d = base.shape[1]
+    if tuple(base.shape) != (2, d) or tuple(Wc.shape) != (d // 8, d):
+        raise ValueError(f"base must be [2, d] and Wc [d/8, d], got {tuple(base.shape)} and {tuple(Wc.shape)}")
+    h = ctypes.c_void_p()
+    _check(lib().dflash_conv2_init(_ptr(base, torch.bfloat16, "base"), _ptr(Wc, torch.bfloat16, "Wc"), d,
+                                   ctypes.byref(h)), "dflash_conv2_init")
+    return h
+
+
+def dflash_conv2_run(handle, X, Y, stream=None):
+    """Y [B, S, d] = the convolution of the blocks X [B, S, d] (bf16, device)."""
+    import torch
+    B, S, d = X.shape
+    if tuple(Y.shape) != (B, S, d):
+        raise ValueError("Y must have X's shape")
+    _check(lib().dflash_conv2_run(handle, _ptr(X, torch.bfloat16, "X"), B, S, _ptr(Y, torch.bfloat16, "Y"),
+                                  _stream(stream)), "dflash_conv2_run")
+
+
+def dflash_conv2_sync_status(handle, stream=None):
+    _check(lib().dflash_conv2_sync_status(handle, _stream(stream)), "dflash_conv2_sync_status")
+
+
+def dflash_conv2_destroy(handle):
+    _check(lib().dflash_conv2_destroy(handle), "dflash_conv2_destroy")
+
+
+class Conv2:
+    """Owns a convolution handle (convenience only)."""
+
+    def __init__(self, base, Wc):
+        self.h = dflash_conv2_init(base, Wc)
+        self._weights = (base, Wc)  # the handle borrows them: keep them alive with it
+
+    def __call__(self, X, Y=None, stream=None):
+        import torch
+        if Y is None:
+            Y = torch.empty_like(X)
+        dflash_conv2_run(self.h, X, Y, stream=stream)
+        return Y
+
+    def close(self):
+        if self.h is not None:
+            dflash_conv2_destroy(self.h)
+            self.h = None
+            self._weights = None
 
     def __enter__(self):
         return self

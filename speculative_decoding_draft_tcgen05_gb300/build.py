@@ -44,7 +44,7 @@ def _stale(lib: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = sources()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    headers.append(os.path.join(INCLUDE, "dflash_select.h"))
+    headers += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     if not force and not _stale(LIB, srcs + headers + [os.path.abspath(__file__)]):
         return LIB
     os.makedirs(BUILD, exist_ok=True)

@@ -221,3 +221,26 @@ def bf16_bits(t: torch.Tensor):
     """The raw bf16 bit patterns of a CPU tensor as a numpy uint16 array (no copy of values)."""
     assert t.dtype == torch.bfloat16
     return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+@dataclass
+class ConvInputs:
+    """One two-tap dynamic convolution and the blocks it runs over (bf16, CPU)."""
+    X: torch.Tensor     # [B, S, d] blocks: the last verified token's row, then the draft rows
+    base: torch.Tensor  # [2, d] base kernels (tap 0: current row, tap 1: the row before)
+    Wc: torch.Tensor    # [d/8, d] correction weights, row 2g + i = tap i of channel group g
+
+
+def make_conv_inputs(B: int, S: int, d: int, seed: int) -> ConvInputs:
+    """Seeded inputs of the drafter's two-tap convolution at a workload's shape
+    (blocks of S = L + 1 rows). Draw order and distributions:
+      X    [B, S, d] ~ N(0, 1)               (hidden states)
+      base [2, d]:   tap 0 ~ 1 + N(0, 0.1), tap 1 ~ N(0, 0.1)
+      Wc   [d/8, d] ~ N(0, 0.1 / sqrt(d))    (a small correction)
+    all rounded to bf16."""
+    g = torch.Generator().manual_seed(seed)
+    X = torch.randn(B, S, d, generator=g).to(torch.bfloat16)
+    base = torch.randn(2, d, generator=g) * 0.1
+    base[0] += 1.0
+    Wc = torch.randn(d // 8, d, generator=g) * (0.1 / math.sqrt(d))
+    return ConvInputs(X=X, base=base.to(torch.bfloat16), Wc=Wc.to(torch.bfloat16))

@@ -1,5 +1,5 @@
 """The C-ABI library builds for sm_103a, loads without a GPU, and exports
-every entry point that include/dflash_select.h declares (no compute calls)."""
+every entry point that the headers under include/ declare (no compute calls)."""
 import ctypes
 import os
 import re
@@ -7,19 +7,24 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "dflash_select.h")
+INCLUDE = os.path.join(ROOT, "include")
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dflash_\w+)\s*\(", text)))
+    names = set()
+    for f in sorted(os.listdir(INCLUDE)):
+        if f.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, f)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(dflash_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("dflash_select_init", "dflash_select_run", "dflash_verify_prefix", "dflash_select_destroy",
-                     "dflash_last_error", "dflash_select_sync_status", "dflash_select_step_host"):
+                     "dflash_last_error", "dflash_select_sync_status", "dflash_select_step_host",
+                     "dflash_select_run_sampled", "dflash_verify_rejection", "dflash_conv2_init", "dflash_conv2_run",
+                     "dflash_conv2_sync_status", "dflash_conv2_destroy"):
         assert required in names
 
 
