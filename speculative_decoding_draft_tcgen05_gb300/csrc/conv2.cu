@@ -19,8 +19,8 @@
 //      (g = c / 16; X[p-1] = 0 at a block's first row): two threads per
 //      (row, group), 8 channels each, 16-byte loads and stores, so a warp
 //      reads and writes 512 contiguous bytes of a row.
-// With at most 32 rows corr is a matrix-vector product bound by the Wc read,
-// and conv2_small_kernel does it on CUDA cores instead (see there).
+// With at most 8 rows (one block) corr is a matrix-vector product bound by the
+// Wc read, and conv2_small_kernel does it on CUDA cores instead (see there).
 // Warp roles of conv2_kernel: warp 0 lane 0 issues TMA copies, warp 1 lane 0 owns TMEM and
 // issues the MMAs, warps 0-3 move the accumulator from TMEM to shared memory,
 // and all 8 warps run the epilogue. Every pipeline wait is bounded.
@@ -365,54 +365,86 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv2_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------------------
-// Few rows (P <= 32, e.g. one or a few blocks): corr is a matrix-vector product
-// bound by reading Wc, so CUDA cores do it without a tensor-core pipeline. One
-// CTA per channel group g: its two Wc rows are loaded before the dependency
-// wait (weights), every thread then takes a strided share of d for all P rows,
-// and after a fixed-order block reduction 2P threads write the group's 16
-// channels of every row.
+// Few rows (P <= 8: one block): corr is a matrix-vector product
+// bound by reading Wc, so CUDA cores do it without a tensor-core pipeline. A
+// CTA takes NG channel groups: their 2 NG Wc rows (contiguous in memory) are
+// bulk-copied into shared memory before the dependency wait (they are
+// weights), then every thread takes a strided share of d for all P rows and
+// all 2 NG rows, and after a fixed-order block reduction one thread per
+// (row, group, half) writes 8 channels.
 constexpr int kSmallThreads = 256;
-constexpr int kSmallMaxU = 8;  // 16-byte pieces of a Wc row per thread: d <= 8 * 8 * 256
+constexpr int kSmallAcc = 64;   // PM * 2 NG accumulators per thread
+constexpr int kSmallRows = 8;   // the few-row kernel's limit (measured: beyond 8 rows the tcgen05 kernel is faster)
 
-template <int PM>
+// 1D bulk copy global -> this CTA's shared memory, counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+template <int PM, int NG>
 __global__ void __launch_bounds__(kSmallThreads) conv2_small_kernel(const __nv_bfloat16 *__restrict__ x,
                                                                     const __nv_bfloat16 *__restrict__ base,
                                                                     const __nv_bfloat16 *__restrict__ Wc,
-                                                                    __nv_bfloat16 *__restrict__ y, int P, int S, int d)
+                                                                    __nv_bfloat16 *__restrict__ y, int P, int S, int d,
+                                                                    int *err)
 {
-    __shared__ float part[kSmallThreads / 32][2 * PM];
-    __shared__ float corr[2 * PM];
-    const int g = blockIdx.x;
+    static_assert(PM * 2 * NG <= kSmallAcc, "accumulators per thread");
+    extern __shared__ __align__(16) uint8_t wsm[];  // Wc rows [2 NG][d] bf16
+    __shared__ float part[kSmallThreads / 32][2 * NG * PM];
+    __shared__ float corr[2 * NG * PM];
+    __shared__ __align__(8) uint64_t bar_w;
+    __shared__ int abort_flag;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nu = d / 8;
-    const uint4 *w0 = reinterpret_cast<const uint4 *>(Wc + static_cast<size_t>(2 * g) * d);
-    const uint4 *w1 = reinterpret_cast<const uint4 *>(Wc + static_cast<size_t>(2 * g + 1) * d);
-    uint4 wa[kSmallMaxU], wb[kSmallMaxU];
-#pragma unroll
-    for (int j = 0; j < kSmallMaxU; ++j) {
-        const int u = tid + j * kSmallThreads;
-        wa[j] = u < nu ? __ldg(w0 + u) : make_uint4(0u, 0u, 0u, 0u);
-        wb[j] = u < nu ? __ldg(w1 + u) : make_uint4(0u, 0u, 0u, 0u);
+    const int G = d / 16;
+    const int g0 = blockIdx.x * NG;
+    const int ng = G - g0 < NG ? G - g0 : NG;  // groups of this CTA
+    const int nu = d / 8;                     // 16-byte pieces of a row
+    const uint32_t bar = smem_u32(&bar_w);
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
     }
-    // the epilogue's base kernels (thread e < 2P: row e / 2, channels 8 (e % 2) ..)
-    const int eh = tid & 1;
-    const size_t ch = static_cast<size_t>(g) * 16 + 8 * eh;
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t row_bytes = static_cast<uint32_t>(d) * 2;
+        mbar_arrive_expect_tx(bar, 2u * ng * row_bytes);
+        for (int r = 0; r < 2 * ng; ++r)
+            bulk_copy_g2s(smem_u32(wsm) + r * row_bytes, Wc + static_cast<size_t>(2 * g0 + r) * d, row_bytes, bar);
+    }
+    // this thread's output piece: row er, group g0 + eg, channels 8 eh .. 8 eh + 7
+    const int eh = tid & 1, eg = (tid >> 1) % NG, er = tid / (2 * NG);
+    const bool epi = er < P && eg < ng;
+    const size_t ch = static_cast<size_t>(g0 + (epi ? eg : 0)) * 16 + 8 * eh;
     float b0[8], b1[8];
     bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(base + ch)), b0);
     bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(base + d + ch)), b1);
     pdl_trigger();
     pdl_wait();
+    uint4 xv = make_uint4(0u, 0u, 0u, 0u), pv = make_uint4(0u, 0u, 0u, 0u);
+    if (epi) {
+        xv = *reinterpret_cast<const uint4 *>(x + static_cast<size_t>(er) * d + ch);
+        if (er % S != 0) pv = *reinterpret_cast<const uint4 *>(x + static_cast<size_t>(er - 1) * d + ch);
+    }
+    bool timed_out = false;
+    if (!mbar_wait(bar, 0, &abort_flag, false)) {  // then wait once more for the copies in flight
+        timed_out = true;
+        mbar_wait(bar, 0, &abort_flag, false);
+    }
 
-    float a0[PM], a1[PM];
+    float acc[PM][2 * NG];
 #pragma unroll
-    for (int r = 0; r < PM; ++r) a0[r] = a1[r] = 0.f;
+    for (int r = 0; r < PM; ++r)
 #pragma unroll
-    for (int j = 0; j < kSmallMaxU; ++j) {
-        const int u = tid + j * kSmallThreads;
-        if (u >= nu) break;
-        float fa[8], fb[8];
-        bf16x8_to_f32(wa[j], fa);
-        bf16x8_to_f32(wb[j], fb);
+        for (int q = 0; q < 2 * NG; ++q) acc[r][q] = 0.f;
+    const uint4 *w4 = reinterpret_cast<const uint4 *>(wsm);
+    for (int u = tid; u < nu; u += kSmallThreads) {
+        float fw[2 * NG][8];
+#pragma unroll
+        for (int q = 0; q < 2 * NG; ++q) bf16x8_to_f32(q < 2 * ng ? w4[q * nu + u] : make_uint4(0u, 0u, 0u, 0u), fw[q]);
 #pragma unroll
         for (int r = 0; r < PM; ++r) {
             if (r >= P) break;
@@ -420,42 +452,30 @@ __global__ void __launch_bounds__(kSmallThreads) conv2_small_kernel(const __nv_b
             bf16x8_to_f32(*reinterpret_cast<const uint4 *>(x + static_cast<size_t>(r) * d + 8 * static_cast<size_t>(u)),
                           fx);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                a0[r] = fmaf(fa[k], fx[k], a0[r]);
-                a1[r] = fmaf(fb[k], fx[k], a1[r]);
-            }
+            for (int q = 0; q < 2 * NG; ++q)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[r][q] = fmaf(fw[q][k], fx[k], acc[r][q]);
         }
-    }
-    // this row's X for the epilogue, loaded while the reduction runs
-    const int er = tid >> 1;
-    uint4 xv = make_uint4(0u, 0u, 0u, 0u), pv = make_uint4(0u, 0u, 0u, 0u);
-    if (er < P) {
-        xv = *reinterpret_cast<const uint4 *>(x + static_cast<size_t>(er) * d + ch);
-        if (er % S != 0) pv = *reinterpret_cast<const uint4 *>(x + static_cast<size_t>(er - 1) * d + ch);
     }
 #pragma unroll
-    for (int r = 0; r < PM; ++r) {
-        float v0 = a0[r], v1 = a1[r];
+    for (int r = 0; r < PM; ++r)
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, off);
-            v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, off);
+        for (int q = 0; q < 2 * NG; ++q) {
+            float v = acc[r][q];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+            if (lane == 0) part[warp][r * 2 * NG + q] = v;
         }
-        if (lane == 0) {
-            part[warp][2 * r] = v0;
-            part[warp][2 * r + 1] = v1;
-        }
-    }
     __syncthreads();
-    if (tid < 2 * PM) {
+    if (tid < 2 * NG * PM) {
         float sum = 0.f;
 #pragma unroll
         for (int w = 0; w < kSmallThreads / 32; ++w) sum += part[w][tid];  // warp order
         corr[tid] = sum;
     }
     __syncthreads();
-    if (er < P) {
-        const float c0 = corr[2 * er], c1 = corr[2 * er + 1];
+    if (epi) {
+        const float c0 = corr[er * 2 * NG + 2 * eg], c1 = corr[er * 2 * NG + 2 * eg + 1];
         float fx[8], fp[8];
         bf16x8_to_f32(xv, fx);
         bf16x8_to_f32(pv, fp);
@@ -469,6 +489,24 @@ __global__ void __launch_bounds__(kSmallThreads) conv2_small_kernel(const __nv_b
         }
         *reinterpret_cast<uint4 *>(y + static_cast<size_t>(er) * d + ch) = make_uint4(out[0], out[1], out[2], out[3]);
     }
+    if (timed_out && tid == 0) atomicOr(err, DEV_ERR_TIMEOUT);
+}
+
+template <int PM, int NG>
+cudaError_t launch_small(const __nv_bfloat16 *x, const __nv_bfloat16 *base, const __nv_bfloat16 *Wc, __nv_bfloat16 *y,
+                         int P, int S, int d, int *err, cudaStream_t s)
+{
+    const size_t smem = static_cast<size_t>(2 * NG) * d * 2;
+    const int G = d / 16;
+    return launch_ex(conv2_small_kernel<PM, NG>, dim3((G + NG - 1) / NG), dim3(kSmallThreads), smem, s, 1, x, base, Wc,
+                     y, P, S, d, err);
+}
+
+// Lets the few-row kernel take the Wc rows it needs (up to 64 KB).
+cudaError_t prepare_small()
+{
+    return cudaFuncSetAttribute(conv2_small_kernel<kSmallRows, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                64 * 1024);
 }
 
 }  // namespace
@@ -531,7 +569,7 @@ extern "C" dflash_status dflash_conv2_init(const void *base, const void *Wc, int
         delete c;
         return st;
     }
-    if (dfl::set_max_dynamic_smem(dfl::conv2_kernel, c->smem_optin) != cudaSuccess ||
+    if (dfl::set_max_dynamic_smem(dfl::conv2_kernel, c->smem_optin) != cudaSuccess || dfl::prepare_small() != cudaSuccess ||
         cudaMalloc(&c->err, sizeof(int)) != cudaSuccess || cudaMemset(c->err, 0, sizeof(int)) != cudaSuccess) {
         if (c->err) cudaFree(c->err);
         delete c;
@@ -557,20 +595,11 @@ extern "C" dflash_status dflash_conv2_run(dflash_conv2_handle h, const void *X, 
     if (xa < ya + bytes && ya < xa + bytes) return conv_fail(DFLASH_ERR_INVALID_ARG, "Y must not overlap X");
     const int P = static_cast<int>(P64);
 
-    if (P <= 32) {  // a matrix-vector product: CUDA cores, one CTA per channel group
-        const cudaStream_t s = static_cast<cudaStream_t>(stream);
-        const dim3 grid(d / 16), block(dfl::kSmallThreads);
-        const auto *xb = static_cast<const __nv_bfloat16 *>(X);
-        const auto *bb = static_cast<const __nv_bfloat16 *>(h->base);
-        const auto *wb = static_cast<const __nv_bfloat16 *>(h->Wc);
-        auto *yb = static_cast<__nv_bfloat16 *>(Y);
-        cudaError_t e;
-        if (P <= 8)
-            e = dfl::launch_ex(dfl::conv2_small_kernel<8>, grid, block, 0, s, 1, xb, bb, wb, yb, P, S, d);
-        else if (P <= 16)
-            e = dfl::launch_ex(dfl::conv2_small_kernel<16>, grid, block, 0, s, 1, xb, bb, wb, yb, P, S, d);
-        else
-            e = dfl::launch_ex(dfl::conv2_small_kernel<32>, grid, block, 0, s, 1, xb, bb, wb, yb, P, S, d);
+    if (P <= dfl::kSmallRows) {  // a matrix-vector product: CUDA cores, one channel group per CTA
+        const cudaError_t e = dfl::launch_small<dfl::kSmallRows, 1>(
+            static_cast<const __nv_bfloat16 *>(X), static_cast<const __nv_bfloat16 *>(h->base),
+            static_cast<const __nv_bfloat16 *>(h->Wc), static_cast<__nv_bfloat16 *>(Y), P, S, d, h->err,
+            static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return conv_fail(DFLASH_ERR_CUDA, "convolution launch failed (error %lld)", e);
         return DFLASH_OK;
     }

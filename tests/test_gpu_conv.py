@@ -43,14 +43,16 @@ def _check(gpu, ref):
 
 
 @pytest.mark.parametrize("B,S,d", [
-    # up to 32 rows: the CUDA-core kernel
+    # up to 8 rows: the CUDA-core kernel
     (1, 8, 128),      # one block, d = 128
-    (2, 8, 2560),     # Qwen3-4B width, batch 2
+    (1, 8, 2560),     # Qwen3-4B width, one block
     (1, 8, 5120),     # 27B-class width
-    (4, 8, 2560),     # 32 rows, the largest of that kernel
     (3, 1, 256),      # S = 1: every row starts a block
+    (1, 5, 16384),    # the widest d (64 KB of Wc rows per CTA)
     # more rows: the tcgen05 kernel
-    (3, 11, 1024),    # 33 rows: 16-wide tiles, d split over a cluster
+    (2, 8, 2560),     # 16 rows: a 16-wide tile, d split over a cluster of 8
+    (4, 8, 2560),     # 32 rows
+    (3, 11, 1024),    # 33 rows: three 16-wide tiles
     (5, 7, 640),      # ragged rows, 80 Wc rows (one partial Wc tile)
     (40, 8, 2560),    # 320 rows, three Wc tiles (the last ragged)
     (1, 300, 64),     # one long block, d = 64 (a single k-block, no split)
