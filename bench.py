@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tables", action="store_true",
+                    help="precompute A|B for every token at init and gather table rows (a variant)")
     ap.add_argument("--mode", default="max-sum", choices=["max-sum", "sample", "conv"],
                     help="max-sum walk + greedy accept check (default), sampling walk + rejection sampling, or the "
                          "drafter's two-tap dynamic convolution over the workload's blocks")
@@ -131,9 +133,10 @@ def committed_traffic(workload):
         return None
 
 
-def algorithmic_bytes(w, G, N):
+def algorithmic_bytes(w, G, N, tables=False):
     """Bytes the selector must move per step (see the design notes): the whole
-    path and, separately, the lm_head+top-K kernel."""
+    path and, separately, the lm_head+top-K kernel. With precomputed tables the
+    E-row gathers and the W_A/W_B reads become gathers of fp32 A|B table rows."""
     d, V, L, K, B, e = w.d, w.V, w.L, w.K, w.B, w.e
     k1 = (V * d * 2            # lm_head weight, read once
           + e * d * 2          # W_H (the gate rows share the pass)
@@ -143,9 +146,10 @@ def algorithmic_bytes(w, G, N):
     R = L * K + 1
     rest = (G * N * K * 8      # partial lists read by the merge
             + N * K * 8        # merged ids + values
-            + B * R * d * 2    # gathered E rows
-            + 2 * e * d * 2    # W_A, W_B
-            + B * R * 2 * e * 4 * 2  # projections written and read
+            + (B * R * 2 * e * 4 if tables else  # gathered table rows
+               B * R * d * 2      # gathered E rows
+               + 2 * e * d * 2    # W_A, W_B
+               + B * R * 2 * e * 4 * 2)  # projections written and read
             + N * e * 4        # gate read
             + N * K * K * 4    # pair tables written
             + B * (L + 1) * 4 + B * L * 4 * 2 + B * 4 + B * (L + 1) * 4)  # path, target, accept, emitted
@@ -293,7 +297,7 @@ def lmhead_geometry(w, sms):
 def finish_sample_line(args, w, world, rank, ms, prof, clk, sel, launches, extra_bytes, sms):
     """The JSON line of the sampling step (sampling walk + rejection sampling)."""
     N, NT, n_tiles, G = lmhead_geometry(w, sms)
-    k1_bytes, all_bytes = algorithmic_bytes(w, G, N)
+    k1_bytes, all_bytes = algorithmic_bytes(w, G, N, args.tables)
     all_bytes += extra_bytes
     k1_ms, k1_n = prof["lmhead_topk"]
     k1_avg_s = k1_ms / max(1, k1_n) / 1e3
@@ -343,7 +347,8 @@ def run_ours(args):
     stream = torch.cuda.Stream(dev)
     sample = args.mode == "sample"
     sel = pkg.Selector(W, E, WA, WB, WH, L=w.L, K=w.K, max_batch=w.B,
-                       walk=pkg.DFLASH_WALK_SAMPLE if sample else pkg.DFLASH_WALK_VITERBI, temperature=1.0)
+                       walk=pkg.DFLASH_WALK_SAMPLE if sample else pkg.DFLASH_WALK_VITERBI, temperature=1.0,
+                       tables=args.tables)
     out = sel.outputs(w.B, full=False)
     accept = torch.empty(w.B, dtype=torch.int32, device=dev)
     emitted = torch.empty(w.B, w.L + 1, dtype=torch.int32, device=dev)
@@ -440,7 +445,7 @@ def run_ours(args):
     launches_per_step = pkg.dflash_select_launches_per_run(sel.h, w.B) + 1
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     N, NT, n_tiles, G = lmhead_geometry(w, sms)
-    k1_bytes, all_bytes = algorithmic_bytes(w, G, N)
+    k1_bytes, all_bytes = algorithmic_bytes(w, G, N, args.tables)
     k1_ms, k1_n = prof["lmhead_topk"]
     k1_avg_s = k1_ms / max(1, k1_n) / 1e3
     peak, peak_kind = hbm_peak()
@@ -459,6 +464,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.label, "B": w.B, "L": w.L, "K": w.K, "V": w.V, "d": w.d, "e": w.e,
+                       "variant": "precomputed A|B tables" if args.tables else "projections per run (the pages' form)",
                        "seed": w.seed, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (lm_head weight %.0f MB > 129 MB L2), no flush" % (w.V * w.d * 2 / 1e6)},
             "hbm_gbs_step": all_bytes / step_s / 1e9,

@@ -72,6 +72,11 @@ typedef struct {
     int32_t walk;       /* dflash_walk */
     float tie_eps;      /* margin under which tie_flags are raised, e.g. 1e-3 */
     float temperature;  /* > 0; used by DFLASH_WALK_SAMPLE */
+    int32_t tables;     /* 0: compute A(a) and B(b) of the candidates in every run (the pages' form);
+                           1: precompute them for every token at init, [A(v) | B(v)] for v < V as
+                           V x 512 fp32 (311 MB at V = 151,936; one GEMM over E of about a
+                           millisecond), and gather table rows in every run. Same results up to fp32
+                           summation order; a variant of this library, not of the pages. */
 } dflash_select_config;
 
 typedef struct dflash_select_ctx *dflash_select_handle;

@@ -42,7 +42,7 @@ class DflashError(RuntimeError):
 class dflash_select_config(ctypes.Structure):
     _fields_ = [("V", ctypes.c_int64), ("d", ctypes.c_int32), ("L", ctypes.c_int32), ("K", ctypes.c_int32),
                 ("e", ctypes.c_int32), ("max_batch", ctypes.c_int32), ("walk", ctypes.c_int32),
-                ("tie_eps", ctypes.c_float), ("temperature", ctypes.c_float)]
+                ("tie_eps", ctypes.c_float), ("temperature", ctypes.c_float), ("tables", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -120,12 +120,13 @@ def _stream(stream):
 
 
 def dflash_select_init(W, E, W_A, W_B, W_H, *, L: int, K: int, max_batch: int, walk: int = DFLASH_WALK_VITERBI,
-                       tie_eps: float = 1e-3, temperature: float = 1.0, stream=None):
-    """Creates a selector handle over device bf16 weights W [V, d], E [V, d], W_A/W_B/W_H [256, d]."""
+                       tie_eps: float = 1e-3, temperature: float = 1.0, tables: bool = False, stream=None):
+    """Creates a selector handle over device bf16 weights W [V, d], E [V, d], W_A/W_B/W_H [256, d]
+    (tables=True: precompute A|B for every token at init and gather table rows in every run)."""
     import torch
     V, d = W.shape
     cfg = dflash_select_config(V=V, d=d, L=L, K=K, e=W_A.shape[0], max_batch=max_batch, walk=walk,
-                               tie_eps=tie_eps, temperature=temperature)
+                               tie_eps=tie_eps, temperature=temperature, tables=1 if tables else 0)
     h = ctypes.c_void_p()
     _check(lib().dflash_select_init(ctypes.byref(cfg), _ptr(W, torch.bfloat16, "W"), _ptr(E, torch.bfloat16, "E"),
                                     _ptr(W_A, torch.bfloat16, "W_A"), _ptr(W_B, torch.bfloat16, "W_B"),
@@ -314,12 +315,12 @@ class Selector:
     """Owns a handle and the output tensors of one batch size (convenience only)."""
 
     def __init__(self, W, E, W_A, W_B, W_H, *, L, K, max_batch, walk=DFLASH_WALK_VITERBI, tie_eps=1e-3,
-                 temperature=1.0):
+                 temperature=1.0, tables=False):
         import torch
         self.L, self.K, self.max_batch = L, K, max_batch
         self.device = W.device
         self.h = dflash_select_init(W, E, W_A, W_B, W_H, L=L, K=K, max_batch=max_batch, walk=walk, tie_eps=tie_eps,
-                                    temperature=temperature)
+                                    temperature=temperature, tables=tables)
         self._weights = (W, E, W_A, W_B, W_H)  # the handle borrows them: keep them alive with it
         self._torch = torch
 

@@ -137,6 +137,7 @@ struct dflash_select_ctx {
     uint64_t *part = nullptr;
     uint64_t *thr_g = nullptr;  // per-position lm_head thresholds shared by the CTAs
     float *gate = nullptr, *vals = nullptr, *AB = nullptr, *P = nullptr;
+    float *tab = nullptr;  // [V][512] precomputed A|B of every token (cfg.tables)
     int32_t *ids = nullptr;
     unsigned *ticket = nullptr;
     int *err = nullptr;
@@ -195,6 +196,41 @@ const char *dflash_last_error(void)
     return g_last_error.c_str();
 }
 
+// [A(v) | B(v)] = [W_A; W_B] E[v] for every token v, by the projection kernel
+// over the identity list of rows (R = 1: row v is "anchor" v).
+static dflash_status build_tables(dflash_select_ctx *c, cudaStream_t s)
+{
+    const int64_t V = c->cfg.V;
+    CUDA_TRY(cudaMalloc(&c->tab, static_cast<size_t>(V) * 512 * sizeof(float)));
+    std::vector<int32_t> ident(static_cast<size_t>(V));
+    for (int64_t v = 0; v < V; ++v) ident[static_cast<size_t>(v)] = static_cast<int32_t>(v);
+    int32_t *rows = nullptr;
+    CUDA_TRY(cudaMalloc(&rows, static_cast<size_t>(V) * sizeof(int32_t)));
+    cudaError_t e = cudaMemcpyAsync(rows, ident.data(), static_cast<size_t>(V) * sizeof(int32_t),
+                                    cudaMemcpyHostToDevice, s);
+    dfl::ProjParams pp;
+    pp.E = static_cast<const uint16_t *>(c->E);
+    pp.WA = static_cast<const uint16_t *>(c->WA);
+    pp.WB = static_cast<const uint16_t *>(c->WB);
+    pp.ids = rows;  // not read with R = 1
+    pp.anchor = rows;
+    pp.AB = c->tab;
+    pp.err = c->err;
+    pp.V = V;
+    pp.d = c->cfg.d;
+    pp.L = 0;
+    pp.K = c->cfg.K;
+    pp.R = 1;
+    pp.R_total = static_cast<int>(V);
+    pp.ksplit = dfl::projection_ksplit(c->cfg.d, pp.R_total, c->num_sms);
+    pp.kchunk = c->cfg.d / pp.ksplit;
+    if (e == cudaSuccess) e = dfl::launch_projection(pp, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaFree(rows);
+    if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "building the A|B tables failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 static dflash_status check_config(const dflash_select_config *c)
 {
     if (!c) return fail(DFLASH_ERR_INVALID_ARG, "config is NULL");
@@ -213,6 +249,7 @@ static dflash_status check_config(const dflash_select_config *c)
         return fail(DFLASH_ERR_INVALID_ARG, "the sampling walk needs a finite temperature > 0");
     if (!(c->tie_eps >= 0.0f) || !std::isfinite(c->tie_eps))
         return fail(DFLASH_ERR_INVALID_ARG, "tie_eps must be finite and >= 0");
+    if (c->tables != 0 && c->tables != 1) return fail(DFLASH_ERR_INVALID_ARG, "tables must be 0 or 1");
     return ok();
 }
 
@@ -326,6 +363,16 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
         delete c;
         return fail(DFLASH_ERR_CUDA, "workspace initialisation failed: %s", cudaGetErrorString(e));
     }
+    if (cfg->tables) {
+        st = build_tables(c, s);
+        if (st != DFLASH_OK) {
+            cudaFree(c->tab);
+            cudaFreeHost(c->err_host);
+            cudaFree(c->ws);
+            delete c;
+            return st;
+        }
+    }
     *out = c;
     return ok();
 }
@@ -405,6 +452,7 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
         dfl::TailParams tp;
         tp.tm_wa = c->tm_wa;
         tp.tm_wb = c->tm_wb;
+        tp.tab = c->tab;
         tp.part = c->part;
         tp.thr_g = c->thr_g;
         tp.gate = c->gate;
@@ -459,12 +507,18 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
     pp.R_total = pl.R_total;
     pp.ksplit = pl.ksplit;
     pp.kchunk = c->cfg.d / pl.ksplit;
-    prof_begin(c, 2, s);
-    CUDA_TRY(dfl::launch_projection(pp, s));
-    prof_end(c, 2, 2, s);
+    if (!c->tab) {
+        prof_begin(c, 2, s);
+        CUDA_TRY(dfl::launch_projection(pp, s));
+        prof_end(c, 2, 2, s);
+    }
 
     dfl::PairParams q;
     q.AB = c->AB;
+    q.tab = c->tab;
+    q.anchor = anchor;
+    q.err = c->err;
+    q.V = c->cfg.V;
     q.gate = c->gate;
     q.vals = c->vals;
     q.ids = c->ids;
@@ -483,9 +537,10 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
     q.u_walk = u_walk;
     q.q_out = draft_probs;
     q.temperature = c->cfg.temperature;
-    prof_begin(c, 3, s);
+    const int slot = c->tab ? 2 : 3;  // profiling slots are filled in launch order
+    prof_begin(c, slot, s);
     CUDA_TRY(dfl::launch_pair_walk(q, s));
-    prof_end(c, 3, 3, s);
+    prof_end(c, slot, 3, s);
     if (prof_on(c)) ++c->prof_runs;
     return ok();
 }
@@ -628,7 +683,7 @@ dflash_status dflash_select_profile_read(dflash_select_handle h, double *ms_tota
 int32_t dflash_select_launches_per_run(dflash_select_handle h, int32_t B)
 {
     if (!h || B <= 0 || B > h->cfg.max_batch) return 0;
-    return h->plan(B).fused_tail ? 2 : 4;
+    return h->plan(B).fused_tail ? 2 : (h->tab ? 3 : 4);
 }
 
 dflash_status dflash_select_destroy(dflash_select_handle h)
@@ -646,6 +701,7 @@ dflash_status dflash_select_destroy(dflash_select_handle h)
     for (auto &x : h->ev) cudaEventDestroy(x);
     cudaFreeHost(h->err_host);
     cudaFree(h->ws);
+    cudaFree(h->tab);
     delete h;
     return st;
 }

@@ -107,7 +107,11 @@ int projection_ksplit(int d, int R_total, int num_sms);
 
 // ---- pair tables and the walk ----
 struct PairParams {
-    const float *AB;      // [B * R][512]
+    const float *AB;      // [B * R][512], or NULL with tab
+    const float *tab;     // [V][512] precomputed A|B of every token (NULL: use AB)
+    const int32_t *anchor;  // [B] (read with tab)
+    int *err;
+    int64_t V;
     const float *gate;    // [B * L][256]
     const float *vals;    // [B, L, K]
     const int32_t *ids;   // [B, L, K]
@@ -128,6 +132,7 @@ cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s);
 // ---- fused tail for small batches: merge + projections + pair tables + walk ----
 struct TailParams {
     CUtensorMap tm_wa, tm_wb;  // W_A, W_B [256, d] bf16, box 64 x 256, 128B swizzle
+    const float *tab;          // [V][512] precomputed A|B of every token (NULL: project in the kernel)
     const uint64_t *part;      // [G][N][K] partial top-K keys
     uint64_t *thr_g;           // [N] lm_head thresholds, reset here for the next pass
     const float *gate;         // [N][256]

@@ -265,10 +265,29 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
         const size_t rowB0 = static_cast<size_t>(b) * R + 1 + t * K;
         float a[K], bb[K];
         const float gk = p.gate[pos * kEmbed + k];
+        if (p.tab) {  // precomputed A|B rows, found by token
+            const int32_t *cur = p.ids + pos * K;
+            int32_t x0 = 0;
+            if (t == 0) {
+                x0 = p.anchor[b];
+                if (x0 < 0 || static_cast<int64_t>(x0) >= p.V) {
+                    if (tid == 0) atomicOr(p.err, DEV_ERR_TOKEN);
+                    x0 = 0;
+                }
+            }
 #pragma unroll
-        for (int i = 0; i < K; ++i) a[i] = (i < n_prev) ? p.AB[(rowA0 + i) * 512 + k] : 0.f;
+            for (int i = 0; i < K; ++i) {
+                const int32_t tok = (t == 0) ? x0 : cur[i - K];  // candidates of t-1
+                a[i] = (i < n_prev) ? __ldg(p.tab + static_cast<size_t>(tok) * 512 + k) : 0.f;
+            }
 #pragma unroll
-        for (int j = 0; j < K; ++j) bb[j] = p.AB[(rowB0 + j) * 512 + kEmbed + k];
+            for (int j = 0; j < K; ++j) bb[j] = __ldg(p.tab + static_cast<size_t>(cur[j]) * 512 + kEmbed + k);
+        } else {
+#pragma unroll
+            for (int i = 0; i < K; ++i) a[i] = (i < n_prev) ? p.AB[(rowA0 + i) * 512 + k] : 0.f;
+#pragma unroll
+            for (int j = 0; j < K; ++j) bb[j] = p.AB[(rowB0 + j) * 512 + kEmbed + k];
+        }
         const float v = (tid < K) ? p.vals[pos * K + tid] : 0.f;
 #pragma unroll
         for (int i = 0; i < K; ++i) Agt[k * K + i] = a[i] * gk;

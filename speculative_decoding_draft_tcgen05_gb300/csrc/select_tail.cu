@@ -25,6 +25,9 @@
 //      each CTA forms its partial pair dot products; rank 0 sums those (rank
 //      order) and adds U_t(b): the table S_t;
 //   5. the last cluster of a sequence (atomic ticket, no waiting) walks.
+// With precomputed tables [A(v) | B(v)] for every token (a handle option),
+// steps 1 and 3 are replaced by a gather: each CTA reads its 256/cs columns of
+// the 2K candidates' table rows (no weights, no MMA, one cluster barrier less).
 // Every summation order is fixed, so results are deterministic.
 #include <cooperative_groups.h>
 
@@ -138,8 +141,9 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
     }
     __syncthreads();
     pdl_trigger();
+    const bool tab = p.tab != nullptr;  // precomputed A|B rows: no projections here
     const int pre = nkb < S ? nkb : S;
-    if (tid == 0) {
+    if (tid == 0 && !tab) {
         tma_prefetch_desc(&p.tm_wa);
         tma_prefetch_desc(&p.tm_wb);
         const uint64_t pol = l2_policy_evict_last();  // every cluster reads the same slices
@@ -242,125 +246,153 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
     }
     __syncthreads();
 
-    // ---------------- 2. partial projections over this CTA's slice of d
-    auto load_e = [&](int kb, int s) {
-        const uint32_t et = base + s * lay.stage + 2 * kWTileBytes;
-        for (int i = tid; i < 2 * K * 8; i += 256) {
-            const int r = i >> 3, c = i & 7;
-            const int tok = rowtok[r];
-            const uint16_t *src = p.E + static_cast<size_t>(tok < 0 ? 0 : tok) * p.d + k0 + kb * 64 + c * 8;
-            cp_async16(et + swz(r, c), src, tok < 0 ? 0u : 16u);
-        }
-    };
-#pragma unroll
-    for (int s = 0; s < S; ++s) {
-        if (s < nkb) load_e(s, s);
-        cp_async_commit();
-    }
-    const int part = warp >> 2;  // 0: A = W_A x previous rows, 1: B = W_B x current rows
-    const int wm = warp & 3;     // 64 output columns each
-    float acc[4][K / 8][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < K / 8; ++j)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[i][j][k] = 0.f;
-
-    for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % S;
-        cp_async_wait<S - 1>();
-        if (!mbar_wait(bar_full + 8u * s, static_cast<uint32_t>(kb / S) & 1u, abort_flag, false))
-            atomicOr(p.err, DEV_ERR_TIMEOUT);
-        __syncthreads();
-        const uint32_t wt = base + s * lay.stage + part * kWTileBytes;
-        const uint32_t et = base + s * lay.stage + 2 * kWTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            uint32_t af[4][4], bf[K / 16][4];
-#pragma unroll
-            for (int mi = 0; mi < 4; ++mi)
-                ldmatrix_x4(wt + swz(wm * 64 + mi * 16 + (lane & 15), kk * 2 + (lane >> 4)), af[mi]);
-#pragma unroll
-            for (int nj = 0; nj < K / 16; ++nj)
-                ldmatrix_x4(et + swz(part * K + nj * 16 + (lane & 7) + ((lane >> 4) << 3), kk * 2 + ((lane >> 3) & 1)),
-                            bf[nj]);
-#pragma unroll
-            for (int mi = 0; mi < 4; ++mi)
-#pragma unroll
-                for (int ni = 0; ni < K / 8; ++ni)
-                    mma_16816(acc[mi][ni], af[mi], bf[ni >> 1][(ni & 1) * 2], bf[ni >> 1][(ni & 1) * 2 + 1]);
-        }
-        __syncthreads();
-        const int nxt = kb + S;
-        if (nxt < nkb) {
-            if (tid == 0) {
-                const uint32_t st = base + s * lay.stage;
-                const uint64_t pol = l2_policy_evict_last();
-                mbar_arrive_expect_tx(bar_full + 8u * s, 2 * kWTileBytes);
-                tma_load_2d(st, &p.tm_wa, k0 + nxt * 64, 0, bar_full + 8u * s, pol);
-                tma_load_2d(st + kWTileBytes, &p.tm_wb, k0 + nxt * 64, 0, bar_full + 8u * s, pol);
-            }
-            load_e(nxt, s);
-        }
-        cp_async_commit();
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-
-    // partial results as Pa[row][column]: rows 0..K-1 = A of the previous
-    // candidates, K..2K-1 = B of the current ones; 256 columns (+4 padding)
-    constexpr int kPaStride = kEmbed + 4;
-    float *const Pa = reinterpret_cast<float *>(gbase);
-    {
-        const int g = lane >> 2, t4 = lane & 3;
-#pragma unroll
-        for (int mi = 0; mi < 4; ++mi)
-#pragma unroll
-            for (int ni = 0; ni < K / 8; ++ni) {
-                const int o = wm * 64 + mi * 16 + g;
-                const int r = part * K + ni * 8 + 2 * t4;
-                Pa[r * kPaStride + o] = acc[mi][ni][0];
-                Pa[(r + 1) * kPaStride + o] = acc[mi][ni][1];
-                Pa[r * kPaStride + o + 8] = acc[mi][ni][2];
-                Pa[(r + 1) * kPaStride + o + 8] = acc[mi][ni][3];
-            }
-    }
-    cluster.sync();
-
-    // ---------------- 3. sum the partials of this CTA's 256/cs columns;
-    // A rows times g_t
+    // the 256/cs columns of A (rows 0..K-1, times g_t) and B (rows K..2K-1)
+    // that this CTA owns, as Red[row][column]
     const int es = kEmbed / cs, e0 = rank * es;
     const int rs = es + kRedPad;
-    float *const Red = Pa + 2 * K * kPaStride;  // [2K][es + pad], after this CTA's Pa
-    for (int i = tid; i < 2 * K * (es / 4); i += 256) {
-        const int r = i / (es / 4), e4 = i % (es / 4);
-        const int col = e0 + e4 * 4;
-        float4 v[8];
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq)
-            if (qq < cs)
-                v[qq] = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(Pa, qq) + r * kPaStride + col);
-        float4 sum = v[0];
-#pragma unroll
-        for (int qq = 1; qq < 8; ++qq)
-            if (qq < cs) {
-                sum.x += v[qq].x;
-                sum.y += v[qq].y;
-                sum.z += v[qq].z;
-                sum.w += v[qq].w;
+    float *Red;
+    if (tab) {
+        // ---------------- 2'. gather the rows from the precomputed table
+        Red = reinterpret_cast<float *>(gbase);
+        for (int i = tid; i < 2 * K * (es / 4); i += 256) {
+            const int r = i / (es / 4), e4 = i % (es / 4);
+            const int col = e0 + e4 * 4;
+            const int tok = rowtok[r];
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (tok >= 0)
+                v = __ldg(reinterpret_cast<const float4 *>(p.tab + static_cast<size_t>(tok) * 512 + (r < K ? 0 : kEmbed) +
+                                                           col));
+            if (r < K) {
+                v.x *= gs[col];
+                v.y *= gs[col + 1];
+                v.z *= gs[col + 2];
+                v.w *= gs[col + 3];
             }
-        if (r < K) {
-            sum.x *= gs[col];
-            sum.y *= gs[col + 1];
-            sum.z *= gs[col + 2];
-            sum.w *= gs[col + 3];
+            float *dst = Red + r * rs + e4 * 4;
+            dst[0] = v.x;
+            dst[1] = v.y;
+            dst[2] = v.z;
+            dst[3] = v.w;
         }
-        float *dst = Red + r * rs + e4 * 4;
-        dst[0] = sum.x;
-        dst[1] = sum.y;
-        dst[2] = sum.z;
-        dst[3] = sum.w;
+    } else {
+        // ---------------- 2. partial projections over this CTA's slice of d
+        auto load_e = [&](int kb, int s) {
+            const uint32_t et = base + s * lay.stage + 2 * kWTileBytes;
+            for (int i = tid; i < 2 * K * 8; i += 256) {
+                const int r = i >> 3, c = i & 7;
+                const int tok = rowtok[r];
+                const uint16_t *src = p.E + static_cast<size_t>(tok < 0 ? 0 : tok) * p.d + k0 + kb * 64 + c * 8;
+                cp_async16(et + swz(r, c), src, tok < 0 ? 0u : 16u);
+            }
+        };
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            if (s < nkb) load_e(s, s);
+            cp_async_commit();
+        }
+        const int part = warp >> 2;  // 0: A = W_A x previous rows, 1: B = W_B x current rows
+        const int wm = warp & 3;     // 64 output columns each
+        float acc[4][K / 8][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < K / 8; ++j)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[i][j][k] = 0.f;
+
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % S;
+            cp_async_wait<S - 1>();
+            if (!mbar_wait(bar_full + 8u * s, static_cast<uint32_t>(kb / S) & 1u, abort_flag, false))
+                atomicOr(p.err, DEV_ERR_TIMEOUT);
+            __syncthreads();
+            const uint32_t wt = base + s * lay.stage + part * kWTileBytes;
+            const uint32_t et = base + s * lay.stage + 2 * kWTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                uint32_t af[4][4], bf[K / 16][4];
+#pragma unroll
+                for (int mi = 0; mi < 4; ++mi)
+                    ldmatrix_x4(wt + swz(wm * 64 + mi * 16 + (lane & 15), kk * 2 + (lane >> 4)), af[mi]);
+#pragma unroll
+                for (int nj = 0; nj < K / 16; ++nj)
+                    ldmatrix_x4(et + swz(part * K + nj * 16 + (lane & 7) + ((lane >> 4) << 3), kk * 2 + ((lane >> 3) & 1)),
+                                bf[nj]);
+#pragma unroll
+                for (int mi = 0; mi < 4; ++mi)
+#pragma unroll
+                    for (int ni = 0; ni < K / 8; ++ni)
+                        mma_16816(acc[mi][ni], af[mi], bf[ni >> 1][(ni & 1) * 2], bf[ni >> 1][(ni & 1) * 2 + 1]);
+            }
+            __syncthreads();
+            const int nxt = kb + S;
+            if (nxt < nkb) {
+                if (tid == 0) {
+                    const uint32_t st = base + s * lay.stage;
+                    const uint64_t pol = l2_policy_evict_last();
+                    mbar_arrive_expect_tx(bar_full + 8u * s, 2 * kWTileBytes);
+                    tma_load_2d(st, &p.tm_wa, k0 + nxt * 64, 0, bar_full + 8u * s, pol);
+                    tma_load_2d(st + kWTileBytes, &p.tm_wb, k0 + nxt * 64, 0, bar_full + 8u * s, pol);
+                }
+                load_e(nxt, s);
+            }
+            cp_async_commit();
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+
+        // partial results as Pa[row][column]: rows 0..K-1 = A of the previous
+        // candidates, K..2K-1 = B of the current ones; 256 columns (+4 padding)
+        constexpr int kPaStride = kEmbed + 4;
+        float *const Pa = reinterpret_cast<float *>(gbase);
+        {
+            const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+            for (int mi = 0; mi < 4; ++mi)
+#pragma unroll
+                for (int ni = 0; ni < K / 8; ++ni) {
+                    const int o = wm * 64 + mi * 16 + g;
+                    const int r = part * K + ni * 8 + 2 * t4;
+                    Pa[r * kPaStride + o] = acc[mi][ni][0];
+                    Pa[(r + 1) * kPaStride + o] = acc[mi][ni][1];
+                    Pa[r * kPaStride + o + 8] = acc[mi][ni][2];
+                    Pa[(r + 1) * kPaStride + o + 8] = acc[mi][ni][3];
+                }
+        }
+        cluster.sync();
+
+        // ---------------- 3. sum the partials of this CTA's 256/cs columns;
+        // A rows times g_t
+        Red = Pa + 2 * K * kPaStride;  // [2K][es + pad], after this CTA's Pa
+        for (int i = tid; i < 2 * K * (es / 4); i += 256) {
+            const int r = i / (es / 4), e4 = i % (es / 4);
+            const int col = e0 + e4 * 4;
+            float4 v[8];
+#pragma unroll
+            for (int qq = 0; qq < 8; ++qq)
+                if (qq < cs)
+                    v[qq] = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(Pa, qq) + r * kPaStride + col);
+            float4 sum = v[0];
+#pragma unroll
+            for (int qq = 1; qq < 8; ++qq)
+                if (qq < cs) {
+                    sum.x += v[qq].x;
+                    sum.y += v[qq].y;
+                    sum.z += v[qq].z;
+                    sum.w += v[qq].w;
+                }
+            if (r < K) {
+                sum.x *= gs[col];
+                sum.y *= gs[col + 1];
+                sum.z *= gs[col + 2];
+                sum.w *= gs[col + 3];
+            }
+            float *dst = Red + r * rs + e4 * 4;
+            dst[0] = sum.x;
+            dst[1] = sum.y;
+            dst[2] = sum.z;
+            dst[3] = sum.w;
+        }
     }
     __syncthreads();
     for (int pr = tid; pr < K * K; pr += 256) {
@@ -445,7 +477,7 @@ int tail_stages(int K, int G, int cs, int smem_optin)
                              static_cast<size_t>(2 * K) * (kEmbed / cs + kRedPad) * 4;
         const size_t walk = static_cast<size_t>(16) * K * K * 4;
         if (reuse > static_cast<size_t>(S) * l.stage || walk > static_cast<size_t>(S) * l.stage) continue;
-        if (l.total + 1024 + 8 * 1024 <= static_cast<size_t>(smem_optin)) return S;  // 8 KB: static shared memory
+        if (l.total + 1024 + 10 * 1024 <= static_cast<size_t>(smem_optin)) return S;  // 10 KB: static shared memory
     }
     return 0;
 }

@@ -20,8 +20,10 @@ namespace dfl {
 
 template <int K>
 struct WalkSmem {
-    uint8_t bp[16 * K];  // back-pointers [t][j]
-    float mg[16 * K];    // gap between the best and second incoming value [t][j]
+    uint8_t bp[16 * K];    // back-pointers [t][j]
+    float mg[16 * K];      // gap between the best and second incoming value [t][j]
+    float delta[2][K];     // max-sum values of the previous and current step
+    int32_t ids[16 * K];   // candidate tokens [t][rank]
     int ranks[16];
     uint8_t flags[16];
 };
@@ -33,12 +35,20 @@ struct SampleArgs {
 };
 
 // Called by every thread of a 256-thread CTA, uniformly. Stages the L tables
-// P_seq [L, K, K] (written by other CTAs of this or an earlier kernel; read
-// around L1) into shared memory Pb, walks them with warp 0 and writes the
-// path tokens ids_seq[t * K + rank_t], the path score and the tie flags
-// (bit 0: the choice at t had a margin below tie_eps -- for the sampling walk,
-// the uniform lay within tie_eps of a CDF boundary; bit 1 at t = L-1: the
-// final choice of the max-sum walk did).
+// P_seq [L, K, K] and the candidates ids_seq [L, K] (written by other CTAs of
+// this or an earlier kernel; read around L1) into shared memory (Pb, ws.ids),
+// walks them and writes the path tokens ids_seq[t * K + rank_t], the path
+// score and the tie flags (bit 0: the choice at t had a margin below tie_eps
+// -- for the sampling walk, the uniform lay within tie_eps of a CDF boundary;
+// bit 1 at t = L-1: the final choice of the max-sum walk did).
+//
+// The max-sum recursion runs on all 256 threads: at each step, thread
+// (j, ig) takes the predecessors i = ig, ig + 256/K, ... of candidate j in
+// increasing order, and the 256/K threads of candidate j (adjacent lanes)
+// combine their (best, first index of best, second best) with shuffles. The
+// result equals the sequential scan over i: the same sums, the smallest rank
+// among equal bests, and a second best equal to the best on a tie. The
+// greedy and sampling walks are sequential over t and run on one warp.
 
 template <int K>
 __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t *ids_seq, int L, int walk,
@@ -47,6 +57,12 @@ __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t 
 {
     const int tid = threadIdx.x;
     {
+        int32_t idv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = tid + u * 256;
+            if (i < L * K) idv[u] = __ldcg(ids_seq + i);
+        }
         const float4 *src = reinterpret_cast<const float4 *>(P_seq);
         float4 *dst = reinterpret_cast<float4 *>(Pb);
         const int n4 = L * K * K / 4;
@@ -63,23 +79,27 @@ __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t 
                 if (i < n4) dst[i] = v[u];
             }
         }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = tid + u * 256;
+            if (i < L * K) ws.ids[i] = idv[u];
+        }
+        if (walk == 0 && tid < K) ws.delta[0][tid] = __ldcg(P_seq + tid);  // delta_0(j) = S_0(x0, j)
     }
     __syncthreads();
-    if (tid >= 32) return;
-    const int lane = tid;
-    const bool active = lane < K;
-    float score;
-
     if (walk == 0) {
-        float delta = active ? Pb[lane] : -INFINITY;
+        constexpr int kIG = 256 / K;  // threads per candidate j
+        constexpr int kIU = K / kIG;  // predecessors per thread
+        const int j = tid / kIG, ig = tid % kIG;
         for (int s = 1; s < L; ++s) {
+            const float *Ps = Pb + s * K * K;
+            const float *dl = ws.delta[(s - 1) & 1];
             float best = -INFINITY, second = -INFINITY;
             int bi = 0;
-            const float *Ps = Pb + s * K * K;
 #pragma unroll
-            for (int i = 0; i < K; ++i) {
-                const float di = __shfl_sync(0xFFFFFFFFu, delta, i);
-                const float v = active ? di + Ps[i * K + lane] : -INFINITY;
+            for (int u = 0; u < kIU; ++u) {
+                const int i = ig + u * kIG;
+                const float v = dl[i] + Ps[i * K + j];
                 if (v > best) {
                     second = best;
                     best = v;
@@ -88,12 +108,30 @@ __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t 
                     second = v;
                 }
             }
-            if (active) {
-                ws.bp[s * K + lane] = static_cast<uint8_t>(bi);
-                ws.mg[s * K + lane] = best - second;
+#pragma unroll
+            for (int off = kIG / 2; off > 0; off >>= 1) {
+                const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+                const float os = __shfl_xor_sync(0xFFFFFFFFu, second, off);
+                second = fmaxf(fmaxf(second, os), fminf(best, ob));
+                if (ob > best || (ob == best && oi < bi)) bi = oi;
+                best = fmaxf(best, ob);
             }
-            delta = best;
+            if (ig == 0) {
+                ws.bp[s * K + j] = static_cast<uint8_t>(bi);
+                ws.mg[s * K + j] = best - second;
+                ws.delta[s & 1][j] = best;
+            }
+            __syncthreads();
         }
+    }
+    if (tid >= 32) return;
+    const int lane = tid;
+    const bool active = lane < K;
+    float score;
+
+    if (walk == 0) {
+        const float delta = active ? ws.delta[(L - 1) & 1][lane] : -INFINITY;
         float bv = active ? delta : -INFINITY;
         int bj = lane;
         for (int off = 16; off > 0; off >>= 1) {
@@ -177,7 +215,7 @@ __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t 
     }
     __syncwarp();
     if (lane < L) {
-        path_out[lane] = __ldcg(ids_seq + lane * K + ws.ranks[lane]);
+        path_out[lane] = ws.ids[lane * K + ws.ranks[lane]];
         if (flags_out) flags_out[lane] = ws.flags[lane];
     }
     if (lane == 0 && score_out) *score_out = score;

@@ -22,7 +22,7 @@ def pkg():
     return p
 
 
-def _full_check(inp, walk=0, seqs=None, max_batch=None):
+def _full_check(inp, walk=0, seqs=None, max_batch=None, tables=False):
     seqs = list(range(inp.wl.B)) if seqs is None else seqs
     orc = parity.run_oracle(inp, seqs, walk=walk)
     # target tokens: planted on the oracle's path for the checked sequences
@@ -32,10 +32,10 @@ def _full_check(inp, walk=0, seqs=None, max_batch=None):
         idx = torch.tensor(seqs, dtype=torch.long)
         path = torch.stack([torch.from_numpy(orc[s]["tokens"]) for s in seqs])
         tgt[idx] = wl.plant_targets(path, inp.target_rand[idx], inp.n0[idx], inp.wl.V)
-    gpu = parity.run_gpu(inp, walk=walk, max_batch=max_batch, targets=tgt)
+    gpu = parity.run_gpu(inp, walk=walk, max_batch=max_batch, targets=tgt, tables=tables)
     targets = {s: tgt[s].numpy() for s in seqs}
     rep = parity.compare(inp, gpu, orc, walk=walk, targets=targets)
-    print(inp.wl.name, "walk", walk, rep)
+    print(inp.wl.name, "walk", walk, "tables" if tables else "", rep)
     return gpu, orc, rep
 
 
