@@ -136,6 +136,8 @@ struct dflash_select_ctx {
     void *ws = nullptr;
     uint64_t *part = nullptr;
     uint64_t *thr_g = nullptr;  // per-position lm_head thresholds shared by the CTAs
+    uint64_t *tmax = nullptr;   // [num_sms][max_batch * L] best logit of each lm_head CTA, epoch-tagged
+    uint32_t epoch = 0;
     float *gate = nullptr, *vals = nullptr, *AB = nullptr, *P = nullptr;
     float *tab = nullptr;  // [V][512] precomputed A|B of every token (cfg.tables)
     int32_t *ids = nullptr;
@@ -314,6 +316,7 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     size_t off = 0;
     const size_t o_part = off; off += up(part_elems * 8);
     const size_t o_thrg = off; off += up(Nmax * 8);
+    const size_t o_tmax = off; off += up(static_cast<size_t>(prop.multiProcessorCount) * Nmax * 8);
     const size_t o_gate = off; off += up(Nmax * dfl::kEmbed * 4);
     const size_t o_ids = off; off += up(Nmax * cfg->K * 4);
     const size_t o_vals = off; off += up(Nmax * cfg->K * 4);
@@ -341,6 +344,7 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     uint8_t *w = static_cast<uint8_t *>(c->ws);
     c->part = reinterpret_cast<uint64_t *>(w + o_part);
     c->thr_g = reinterpret_cast<uint64_t *>(w + o_thrg);
+    c->tmax = reinterpret_cast<uint64_t *>(w + o_tmax);
     c->gate = reinterpret_cast<float *>(w + o_gate);
     c->ids = reinterpret_cast<int32_t *>(w + o_ids);
     c->vals = reinterpret_cast<float *>(w + o_vals);
@@ -442,6 +446,9 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
     lp.part = c->part;
     lp.gate = c->gate;
     lp.thr_g = c->thr_g;
+    lp.tmax = c->tmax;
+    lp.epoch = ++c->epoch;
+    if (lp.epoch == 0) lp.epoch = ++c->epoch;  // 0 is the value of the zeroed workspace
     lp.err = c->err;
 
     prof_begin(c, 0, s);

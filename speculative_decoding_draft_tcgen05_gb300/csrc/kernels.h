@@ -81,6 +81,9 @@ struct LmHeadParams {
     uint64_t *part;   // [ctas_per_ntile][N][K] partial top-K keys
     float *gate;      // [N][256] g_t = W_H h_t
     uint64_t *thr_g;  // [N] best K-th key published by any CTA; zero on entry, reset by the consumer
+    uint64_t *tmax;   // [ctas_per_ntile][N] each CTA's best logit after its first tile, tagged with
+                      // `epoch` in the high word (NULL: not used)
+    uint32_t epoch;   // differs between consecutive runs on the same tmax
     int *err;
 };
 

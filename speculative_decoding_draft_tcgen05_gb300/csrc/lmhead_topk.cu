@@ -76,7 +76,7 @@ __host__ __device__ inline uint32_t tmem_cols_for(int NT)
 }
 
 struct Layout {
-    uint32_t stage_bytes, off_T, off_wscr, off_list, off_thr, off_thrf, off_flags, off_bar, total;
+    uint32_t stage_bytes, off_T, off_wscr, off_list, off_thr, off_thrf, off_rb, off_flags, off_cmask, off_bar, total;
 };
 
 __host__ __device__ inline Layout make_layout(int NT, int K, int stages, int boxes)
@@ -88,8 +88,10 @@ __host__ __device__ inline Layout make_layout(int NT, int K, int stages, int box
     l.off_list = l.off_wscr + 8 * kLmTileM;  // eight epilogue warps x 128 row indices
     l.off_thr = l.off_list + static_cast<uint32_t>(NT) * K * 8;
     l.off_thrf = l.off_thr + static_cast<uint32_t>(NT) * 8;
-    l.off_flags = l.off_thrf + static_cast<uint32_t>(NT) * 4;
-    l.off_bar = l.off_flags + 16;
+    l.off_rb = l.off_thrf + static_cast<uint32_t>(NT) * 4;
+    l.off_flags = l.off_rb + static_cast<uint32_t>(NT) * 8;
+    l.off_cmask = l.off_flags + 16;
+    l.off_bar = l.off_cmask + 16 * 4 * 4;
     // full[S], empty[S], tfull[2], tempty[2], drain, then tmem base + abort flag
     l.total = l.off_bar + 8u * (2u * stages + 5u) + 16u;
     return l;
@@ -112,8 +114,13 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     uint64_t *const thr = reinterpret_cast<uint64_t *>(gbase + lay.off_thr);
     // per position: the logit of the K-th best key so far (-inf until K are held)
     float *const thr_f = reinterpret_cast<float *>(gbase + lay.off_thrf);
+    // per position: a threshold from the other CTAs' best logits (see below)
+    uint64_t *const rb = reinterpret_cast<uint64_t *>(gbase + lay.off_rb);
     // per 16-column chunk: which columns have a surviving logit (3 rotating words)
     volatile uint32_t *const chunk_flags = reinterpret_cast<volatile uint32_t *>(gbase + lay.off_flags);
+    // per column of the current chunk and TMEM lane quadrant: the tile rows whose
+    // logit passes the column's float threshold
+    uint32_t *const cmask = reinterpret_cast<uint32_t *>(gbase + lay.off_cmask);
     const uint32_t bar_full = base + lay.off_bar;
     const uint32_t bar_empty = bar_full + 8u * S;
     const uint32_t bar_tfull = bar_empty + 8u * S;
@@ -297,14 +304,46 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     if (et + h * 256 < nvalid)
                         tg[h] = *reinterpret_cast<volatile const uint64_t *>(p.thr_g + col_base + et + h * 256);
             }
+            // Used where the list upkeep is the bottleneck (many positions per
+            // CTA, measured: from about 100) and the n-tile has enough CTAs to
+            // give K maxima.
+            const bool refresh = p.tmax && !gate && j == 2 && G >= 2 * K && nvalid >= 96;
+            if (refresh) {
+                // Every CTA of this n-tile published its best logit per position
+                // after its first tile. If at least K of them are >= v, then K
+                // logits are >= v, so v bounds the K-th best from below: far
+                // higher than any one CTA's K-th best this early. Each lane takes
+                // the best of its share of the CTAs; v = the K-th best lane.
+                for (int col = ew; col < nvalid; col += 8) {
+                    uint64_t t[5];  // G <= 160 CTAs per n-tile: at most 5 per lane
+#pragma unroll
+                    for (int u2 = 0; u2 < 5; ++u2) {
+                        const int g2 = lane + 32 * u2;
+                        t[u2] = g2 < G ? __ldcg(p.tmax + static_cast<size_t>(g2) * p.N + col_base + col) : 0ull;
+                    }
+                    uint32_t best = 0;
+#pragma unroll
+                    for (int u2 = 0; u2 < 5; ++u2) {
+                        const uint32_t o = static_cast<uint32_t>(t[u2]);
+                        if (static_cast<uint32_t>(t[u2] >> 32) == p.epoch && o > best) best = o;
+                    }
+                    const uint64_t srt = warp_sort_desc(static_cast<uint64_t>(best), lane);
+                    const uint64_t kth = shfl_u64(srt, K - 1);
+                    if (lane == 0) rb[col] = kth << 32;  // any key of that logit value or above passes
+                }
+            }
             const bool got = tmem_warp ? mbar_wait(bar_tfull + 8u * a, u & 1u, abort_flag) : true;
+            if (refresh) named_bar_sync(1, 256);
             if (!gate) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int c = et + h * 256;
-                    if (c < nvalid && tg[h] > thr[c]) {
-                        thr[c] = tg[h];
-                        thr_f[c] = key_val(tg[h]);
+                    if (c < nvalid) {
+                        const uint64_t t = refresh && rb[c] > tg[h] ? rb[c] : tg[h];
+                        if (t > thr[c]) {
+                            thr[c] = t;
+                            thr_f[c] = key_val(t);
+                        }
                     }
                 }
             }
@@ -346,20 +385,18 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                 const int slot = nchunk % 3;
                 ++nchunk;
                 uint32_t mask = 0;
-                if (tmem_warp && static_cast<int64_t>(row0) + row < p.V) {
-                    const float4 *tf4 = reinterpret_cast<const float4 *>(thr_f + c0);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const float4 th4 = tf4[q4];
-                        mask |= (v[4 * q4 + 0] >= th4.x ? 1u : 0u) << (4 * q4 + 0);
-                        mask |= (v[4 * q4 + 1] >= th4.y ? 1u : 0u) << (4 * q4 + 1);
-                        mask |= (v[4 * q4 + 2] >= th4.z ? 1u : 0u) << (4 * q4 + 2);
-                        mask |= (v[4 * q4 + 3] >= th4.w ? 1u : 0u) << (4 * q4 + 3);
-                    }
+                if (tmem_warp) {
+                    const bool rowok = static_cast<int64_t>(row0) + row < p.V;
                     const int vcols = nvalid - c0;
-                    if (vcols < 16) mask &= (1u << vcols) - 1u;
+                    uint32_t mine_cols = 0;
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const unsigned b = __ballot_sync(0xFFFFFFFFu, rowok && jj < vcols && v[jj] >= thr_f[c0 + jj]);
+                        if (lane == jj) mine_cols = b;
+                        mask |= (b ? 1u : 0u) << jj;  // uniform across the warp
+                    }
+                    if (lane < 16) cmask[lane * 4 + q] = mine_cols;
                 }
-                mask = __reduce_or_sync(0xFFFFFFFFu, mask);
                 if (lane == 0 && mask) atomicOr(const_cast<uint32_t *>(&chunk_flags[slot]), mask);
                 named_bar_sync(1, 256);
                 const uint32_t flags = chunk_flags[slot];
@@ -376,16 +413,12 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     const int col = c0 + cc;
                     if (col >= nvalid || !((flags >> cc) & 1u)) continue;  // uniform across the warp
                     uint64_t th = thr[col];
-                    // the column's 128 keys of this tile, four per lane
-                    uint64_t key[4];
-                    unsigned surv[4];
+                    // the tile rows that passed the float filter (from the TMEM warps)
+                    uint32_t surv[4];
                     int total = 0;
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
-                        const int r = qq * 32 + lane;
-                        const int64_t id = static_cast<int64_t>(row0) + r;
-                        key[qq] = (id < p.V) ? make_key(T[cc * kLmTileM + r], static_cast<uint32_t>(id)) : 0ull;
-                        surv[qq] = __ballot_sync(0xFFFFFFFFu, key[qq] > th);
+                        surv[qq] = cmask[cc * 4 + qq];
                         total += __popc(surv[qq]);
                     }
                     const bool loaded = total > 0;
@@ -400,7 +433,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                         int base_i = 0;
 #pragma unroll
                         for (int qq = 0; qq < 4; ++qq) {
-                            if (key[qq] > th) scr[base_i + __popc(surv[qq] & lt)] = static_cast<uint8_t>(qq * 32 + lane);
+                            if ((surv[qq] >> lane) & 1u) scr[base_i + __popc(surv[qq] & lt)] = static_cast<uint8_t>(qq * 32 + lane);
                             base_i += __popc(surv[qq]);
                         }
                         __syncwarp();
@@ -421,9 +454,9 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                         for (int qq = 0; qq < 4; ++qq) {
                             unsigned sv = surv[qq];
                             while (sv) {
-                                const int src = __ffs(sv) - 1;
+                                const int r = qq * 32 + __ffs(sv) - 1;
                                 sv &= sv - 1;
-                                const uint64_t x = shfl_u64(key[qq], src);
+                                const uint64_t x = make_key(T[cc * kLmTileM + r], static_cast<uint32_t>(row0 + r));
                                 if (x > th) {
                                     mine = list_insert(mine, x, lane, K);
                                     const uint64_t kth = shfl_u64(mine, K - 1);
@@ -449,6 +482,16 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
             if (tmem_warp) {
                 tc_fence_before_sync();
                 mbar_arrive(bar_tempty + 8u * a);
+            }
+            if (p.tmax && !gate && j == 0) {
+                named_bar_sync(1, 256);  // the first tile's lists are complete
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int c = et + h * 256;
+                    if (c < nvalid)
+                        p.tmax[static_cast<size_t>(chunk) * p.N + col_base + c] =
+                            (static_cast<uint64_t>(p.epoch) << 32) | (lists[c * K] >> 32);
+                }
             }
         }
         if (!ok) atomicOr(p.err, DEV_ERR_TIMEOUT);

@@ -147,6 +147,8 @@ extern "C" dflash_status dflash_lmhead_topk_noalloc(const void *W_lm, int64_t V,
     p.part = reinterpret_cast<uint64_t *>(dev.scratch + kPartOffset);
     p.gate = nullptr;
     p.thr_g = reinterpret_cast<uint64_t *>(dev.scratch + kThrOffset);
+    p.tmax = nullptr;  // no cross-CTA maxima (they would need per-call scratch)
+    p.epoch = 0;
     p.err = reinterpret_cast<int *>(dev.scratch + kErrOffset);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
