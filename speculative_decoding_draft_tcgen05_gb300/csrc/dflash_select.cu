@@ -160,8 +160,11 @@ struct dflash_select_ctx {
         p.N = B * cfg.L;
         // position tiles of at most 128 up to 256 positions (the per-CTA top-K
         // upkeep grows with the tile's width), 256 beyond
+#ifndef DFL_LM_TILE_POS
+#define DFL_LM_TILE_POS 128
+#endif
         if (p.N <= 256) {
-            p.n_tiles_n = (p.N + 127) / 128;
+            p.n_tiles_n = (p.N + DFL_LM_TILE_POS - 1) / DFL_LM_TILE_POS;
             p.NT = (((p.N + p.n_tiles_n - 1) / p.n_tiles_n) + 15) / 16 * 16;
         } else {
             p.NT = 256;
