@@ -109,7 +109,7 @@ constexpr int kProfileKernels = 5;  // lm_head+top-K, merge, projection, pair+wa
 constexpr int kProfileSlots = 4;    // launches recorded per run
 
 struct Plan {
-    int N, NT, n_tiles_n, G, grid, stages, boxes, R_total, ksplit;
+    int N, NT, n_tiles_n, G, grid, stages, boxes, R_total;
     size_t smem;
     bool fused_tail;  // one clustered kernel for merge + projections + tables + walk
     int tail_cs, tail_S;
@@ -129,6 +129,7 @@ struct dflash_select_ctx {
     int device = 0, num_sms = 0;
     size_t smem_optin = 0;  // opt-in shared memory per block
     CUtensorMap tm_w, tm_gate, tm_h, tm_wa, tm_wb;
+    CUtensorMap tm_pa[3], tm_pb[3];  // W_A, W_B with 64 x {64, 128, 256}-row boxes (projection tiles)
     const void *h_ptr = nullptr;
     int h_rows = -1;
     int m_tiles_vocab = 0, m_tiles_total = 0, R = 0;
@@ -185,7 +186,6 @@ struct dflash_select_ctx {
         p.stages = st;
         p.smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, st, p.boxes);
         p.R_total = B * R;
-        p.ksplit = dfl::projection_ksplit(cfg.d, p.R_total, num_sms);
         p.tail_cs = dfl::tail_cluster_size(cfg.d);
         p.tail_S = dfl::tail_stages(cfg.K, p.G, p.tail_cs, static_cast<int>(smem_optin));
         p.fused_tail = p.n_tiles_n == 1 && p.N * p.tail_cs <= num_sms && p.tail_S > 0;
@@ -214,9 +214,11 @@ static dflash_status build_tables(dflash_select_ctx *c, cudaStream_t s)
     cudaError_t e = cudaMemcpyAsync(rows, ident.data(), static_cast<size_t>(V) * sizeof(int32_t),
                                     cudaMemcpyHostToDevice, s);
     dfl::ProjParams pp;
+    const int nc = dfl::projection_cols(static_cast<int>(V), c->num_sms);
+    const int ti = nc == 64 ? 0 : (nc == 128 ? 1 : 2);
+    pp.tm_wa = c->tm_pa[ti];
+    pp.tm_wb = c->tm_pb[ti];
     pp.E = static_cast<const uint16_t *>(c->E);
-    pp.WA = static_cast<const uint16_t *>(c->WA);
-    pp.WB = static_cast<const uint16_t *>(c->WB);
     pp.ids = rows;  // not read with R = 1
     pp.anchor = rows;
     pp.AB = c->tab;
@@ -227,9 +229,7 @@ static dflash_status build_tables(dflash_select_ctx *c, cudaStream_t s)
     pp.K = c->cfg.K;
     pp.R = 1;
     pp.R_total = static_cast<int>(V);
-    pp.ksplit = dfl::projection_ksplit(c->cfg.d, pp.R_total, c->num_sms);
-    pp.kchunk = c->cfg.d / pp.ksplit;
-    if (e == cudaSuccess) e = dfl::launch_projection(pp, s);
+    if (e == cudaSuccess) e = dfl::launch_projection(pp, nc, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     cudaFree(rows);
     if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "building the A|B tables failed: %s", cudaGetErrorString(e));
@@ -281,6 +281,7 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
 
     CUDA_TRY(dfl::prepare_lmhead(static_cast<int>(prop.sharedMemPerBlockOptin)));
     CUDA_TRY(dfl::prepare_pair_walk(static_cast<int>(prop.sharedMemPerBlockOptin)));
+    CUDA_TRY(dfl::prepare_projection(static_cast<int>(prop.sharedMemPerBlockOptin)));
     CUDA_TRY(dfl::prepare_tail(static_cast<int>(prop.sharedMemPerBlockOptin)));
 
     dflash_select_ctx *c = new (std::nothrow) dflash_select_ctx();
@@ -301,7 +302,13 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     if ((st = make_tmap(&c->tm_w, W_lm, cfg->V, cfg->d, dfl::kLmTileM)) != DFLASH_OK ||
         (st = make_tmap(&c->tm_gate, W_H, dfl::kEmbed, cfg->d, dfl::kLmTileM)) != DFLASH_OK ||
         (st = make_tmap(&c->tm_wa, W_A, dfl::kEmbed, cfg->d, dfl::kEmbed)) != DFLASH_OK ||
-        (st = make_tmap(&c->tm_wb, W_B, dfl::kEmbed, cfg->d, dfl::kEmbed)) != DFLASH_OK) {
+        (st = make_tmap(&c->tm_wb, W_B, dfl::kEmbed, cfg->d, dfl::kEmbed)) != DFLASH_OK ||
+        (st = make_tmap(&c->tm_pa[0], W_A, dfl::kEmbed, cfg->d, 64)) != DFLASH_OK ||
+        (st = make_tmap(&c->tm_pa[1], W_A, dfl::kEmbed, cfg->d, 128)) != DFLASH_OK ||
+        (st = make_tmap(&c->tm_pa[2], W_A, dfl::kEmbed, cfg->d, 256)) != DFLASH_OK ||
+        (st = make_tmap(&c->tm_pb[0], W_B, dfl::kEmbed, cfg->d, 64)) != DFLASH_OK ||
+        (st = make_tmap(&c->tm_pb[1], W_B, dfl::kEmbed, cfg->d, 128)) != DFLASH_OK ||
+        (st = make_tmap(&c->tm_pb[2], W_B, dfl::kEmbed, cfg->d, 256)) != DFLASH_OK) {
         delete c;
         return st;
     }
@@ -502,9 +509,11 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
     prof_end(c, 1, 1, s);
 
     dfl::ProjParams pp;
+    const int nc = dfl::projection_cols(pl.R_total, c->num_sms);
+    const int ti = nc == 64 ? 0 : (nc == 128 ? 1 : 2);
+    pp.tm_wa = c->tm_pa[ti];
+    pp.tm_wb = c->tm_pb[ti];
     pp.E = static_cast<const uint16_t *>(c->E);
-    pp.WA = static_cast<const uint16_t *>(c->WA);
-    pp.WB = static_cast<const uint16_t *>(c->WB);
     pp.ids = c->ids;
     pp.anchor = anchor;
     pp.AB = c->AB;
@@ -515,11 +524,9 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
     pp.K = c->cfg.K;
     pp.R = c->R;
     pp.R_total = pl.R_total;
-    pp.ksplit = pl.ksplit;
-    pp.kchunk = c->cfg.d / pl.ksplit;
     if (!c->tab) {
         prof_begin(c, 2, s);
-        CUDA_TRY(dfl::launch_projection(pp, s));
+        CUDA_TRY(dfl::launch_projection(pp, nc, s));
         prof_end(c, 2, 2, s);
     }
 

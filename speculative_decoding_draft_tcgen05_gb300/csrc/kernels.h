@@ -95,18 +95,23 @@ cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cud
 cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws,
                               float *vals_ws, int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s);
 
-// ---- candidate projections A|B = [W_A; W_B] E[row] (mma.sync, cluster split-K) ----
+// ---- candidate projections A|B = [W_A; W_B] E[row] (tcgen05, projection.cu) ----
 struct ProjParams {
-    const uint16_t *E, *WA, *WB;  // bf16 bits
+    CUtensorMap tm_wa, tm_wb;     // W_A, W_B [256, d] bf16, box 64 x 256, 128B swizzle
+    const uint16_t *E;            // [V, d] bf16 bits
     const int32_t *ids;           // [B, L, K] merged candidates
     const int32_t *anchor;        // [B]
     float *AB;                    // [B * R][512]: cols 0..255 = A, 256..511 = B
     int *err;
     int64_t V;
-    int d, L, K, R, R_total, ksplit, kchunk;
+    int d, L, K, R, R_total;      // gathered row gr: sequence gr / R, row gr % R (0: x0, else a candidate)
 };
-cudaError_t launch_projection(const ProjParams &p, cudaStream_t s);
-int projection_ksplit(int d, int R_total, int num_sms);
+cudaError_t prepare_projection(int smem_optin);
+// Output columns per CTA (64, 128 or 256) for R_total gathered rows: the
+// narrowest whose grid still fits one CTA per SM.
+int projection_cols(int R_total, int num_sms);
+// p.tm_wa / p.tm_wb must have boxes of 64 columns x NC rows.
+cudaError_t launch_projection(const ProjParams &p, int NC, cudaStream_t s);
 
 // ---- pair tables and the walk ----
 struct PairParams {
