@@ -10,8 +10,8 @@
 //
 // The projections A|B of the gathered candidates come from projection.cu.
 // pair_walk_kernel: one CTA per (sequence, position) builds the K x K table in
-//   fp32 (CUDA cores; exact fp32 inputs, no rounding to bf16); the last CTA of
-//   each sequence (atomic ticket, no waiting) runs the walk in one warp.
+//   fp32 (CUDA cores, register-tiled; exact fp32 inputs, no rounding to bf16);
+//   the last CTA of each sequence (atomic ticket, no waiting) runs the walk.
 #include "common.cuh"
 #include "kernels.h"
 #include "walk.cuh"
@@ -81,23 +81,52 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
 
     float *Pt = p.P + pos * K * K;
     float *Po = p.P_out ? p.P_out + pos * K * K : nullptr;
-    for (int e = tid; e < K * K; e += blockDim.x) {
-        const int i = e / K, jj = e % K;
-        float s;
-        if (i < n_prev) {
-            // two partial sums halve the dependent FMA chain
-            float d0 = 0.f, d1 = 0.f;
-#pragma unroll 8
-            for (int k = 0; k < kEmbed; k += 2) {
-                d0 = fmaf(Agt[k * K + i], Bt[k * K + jj], d0);
-                d1 = fmaf(Agt[(k + 1) * K + i], Bt[(k + 1) * K + jj], d1);
+    {
+        // Register tiles: thread (kg, bi, bj) sums components [64 kg, 64 kg + 64)
+        // of the RT x RT pairs (bi RT + r1, bj RT + r2), RT = K / 8, reading RT
+        // values of each operand per component (one vector load each), so shared
+        // memory serves RT^2 FMAs per two loads instead of one FMA per two.
+        constexpr int RT = K / 8;
+        const int kg = tid >> 6, bi = (tid >> 3) & 7, bj = tid & 7;
+        float acc[RT][RT];
+#pragma unroll
+        for (int r1 = 0; r1 < RT; ++r1)
+#pragma unroll
+            for (int r2 = 0; r2 < RT; ++r2) acc[r1][r2] = 0.f;
+#pragma unroll 4
+        for (int k = kg * 64; k < kg * 64 + 64; ++k) {
+            float a[RT], bb[RT];
+            if constexpr (RT == 4) {
+                const float4 av = *reinterpret_cast<const float4 *>(Agt + k * K + bi * RT);
+                const float4 bv = *reinterpret_cast<const float4 *>(Bt + k * K + bj * RT);
+                a[0] = av.x, a[1] = av.y, a[2] = av.z, a[3] = av.w;
+                bb[0] = bv.x, bb[1] = bv.y, bb[2] = bv.z, bb[3] = bv.w;
+            } else {
+                const float2 av = *reinterpret_cast<const float2 *>(Agt + k * K + bi * RT);
+                const float2 bv = *reinterpret_cast<const float2 *>(Bt + k * K + bj * RT);
+                a[0] = av.x, a[1] = av.y;
+                bb[0] = bv.x, bb[1] = bv.y;
             }
-            s = vals[jj] + (d0 + d1);
-        } else {
-            s = -INFINITY;  // only the anchor precedes position 0
+#pragma unroll
+            for (int r1 = 0; r1 < RT; ++r1)
+#pragma unroll
+                for (int r2 = 0; r2 < RT; ++r2) acc[r1][r2] = fmaf(a[r1], bb[r2], acc[r1][r2]);
         }
-        Pt[e] = s;
-        if (Po) Po[e] = s;
+        __syncthreads();  // every thread is done with Agt / Bt
+        float *const part = pw_smem;  // [4 component groups][K * K], over Agt
+#pragma unroll
+        for (int r1 = 0; r1 < RT; ++r1)
+#pragma unroll
+            for (int r2 = 0; r2 < RT; ++r2) part[kg * K * K + (bi * RT + r1) * K + bj * RT + r2] = acc[r1][r2];
+        __syncthreads();
+        for (int e = tid; e < K * K; e += blockDim.x) {
+            const int i = e / K, jj = e % K;
+            // the four component groups in order
+            const float dot = ((part[e] + part[K * K + e]) + part[2 * K * K + e]) + part[3 * K * K + e];
+            const float sc = (i < n_prev) ? vals[jj] + dot : -INFINITY;  // only the anchor precedes position 0
+            Pt[e] = sc;
+            if (Po) Po[e] = sc;
+        }
     }
 
     __syncthreads();
