@@ -113,10 +113,18 @@ def tensor_roofline(flops, avg_s, nbytes, launches, workload):
 
 
 def kernel_src_digest():
+    """sha256 of the lm_head kernel's source: its .cu file, the shared device
+    helpers, and the part of kernels.h up to the other kernels' declarations
+    (launch helper, parameters, launch functions)."""
+    csrc = os.path.join(ROOT, "speculative_decoding_draft_tcgen05_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("lmhead_topk.cu", "common.cuh", "kernels.h"):
-        with open(os.path.join(ROOT, "speculative_decoding_draft_tcgen05_gb300", "csrc", f), "rb") as fh:
+    for f in ("lmhead_topk.cu", "common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
+    with open(os.path.join(csrc, "kernels.h"), "rb") as fh:
+        text = fh.read()
+    cut = text.find(b"// ---- candidate projections")
+    h.update(text if cut < 0 else text[:cut])
     return h.hexdigest()
 
 
