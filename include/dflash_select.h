@@ -224,6 +224,15 @@ dflash_status dflash_select_destroy(dflash_select_handle h);
 /* Message of the last failed call on this thread ("" if none). */
 const char *dflash_last_error(void);
 
+/* Self-test of the bounded pipeline wait (no counterpart in the pages). Every
+ * mbarrier wait of the library's kernels gives up after 1 s, latches the
+ * device error bit 2 (reported as DFLASH_ERR_TIMEOUT) and lets the kernel
+ * return. This launches a one-warp kernel whose wait can never complete, so
+ * the caller can observe that path: after about 1 s `device_status` (one
+ * int32 on the device, zeroed by the caller) has bit 2 set, and the context
+ * stays usable. Errors: INVALID_ARG, CUDA. */
+dflash_status dflash_selftest_wait_timeout(int32_t *device_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

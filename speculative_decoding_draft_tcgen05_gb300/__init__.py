@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
             L.dflash_select_launches_per_run.restype = i32
             L.dflash_select_destroy.argtypes = [P]
             L.dflash_lmhead_topk_noalloc.argtypes = [P, i64, i32, P, i32, i32, P, P, P, P]
+            L.dflash_selftest_wait_timeout.argtypes = [P, P]
             L.dflash_conv2_init.argtypes = [P, P, i32, ctypes.POINTER(P)]
             L.dflash_conv2_run.argtypes = [P, P, i32, i32, P, P]
             L.dflash_conv2_sync_status.argtypes = [P, P]
@@ -82,7 +83,7 @@ def lib() -> ctypes.CDLL:
                       "dflash_select_sync_status", "dflash_select_profile", "dflash_select_profile_read",
                       "dflash_select_destroy", "dflash_lmhead_topk_noalloc", "dflash_select_run_sampled",
                       "dflash_verify_rejection", "dflash_conv2_init", "dflash_conv2_run", "dflash_conv2_sync_status",
-                      "dflash_conv2_destroy"):
+                      "dflash_conv2_destroy", "dflash_selftest_wait_timeout"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -410,3 +411,10 @@ class Conv2:
 
     def __exit__(self, *exc):
         self.close()
+
+
+def dflash_selftest_wait_timeout(device_status, stream=None):
+    """Launches a kernel whose bounded wait runs out (about 1 s); bit 2 of device_status [1] int32 gets set."""
+    import torch
+    _check(lib().dflash_selftest_wait_timeout(_ptr(device_status, torch.int32, "device_status"), _stream(stream)),
+           "dflash_selftest_wait_timeout")
