@@ -14,9 +14,11 @@
 // streamed 64 columns per stage by TMA into 128-byte-swizzled shared memory.
 // Warp roles per CTA (persistent, one CTA per SM):
 //   warp 0      TMA producer (one thread), `stages`-deep ring
-//   warp 1      TMEM owner and MMA issuer (one thread), two accumulators
-//   warps 2..5  epilogue: TMEM -> registers -> transpose through shared
-//               memory -> per-position threshold filter -> warp-sorted insert
+//   warp 1      TMEM owner and MMA issuer (one thread), two or four
+//               accumulators
+//   warps 2..9  epilogue: TMEM -> registers -> per-position threshold filter
+//               -> the survivors into per-position sorted lists (warp-sorted
+//               merges while the lists fill, one thread per position after)
 // Each CTA owns one n-tile and every ctas_per_ntile-th M tile; it writes one
 // sorted partial list of K keys per position, merged by topk_merge_kernel.
 #include "common.cuh"
@@ -31,6 +33,72 @@ constexpr uint32_t kTransposeBytes = 16 * kLmTileM * 4;    // 16 columns x 128 r
 // Up to this many surviving keys per warp are inserted one by one; more are
 // sorted and merged (a sort + merge costs about as much as 6 to 8 inserts).
 constexpr int kInsertLimit = 6;
+// Keys the per-tile path can hold per tile (buckets over the transpose buffer).
+constexpr int kBucketKeys = static_cast<int>(kTransposeBytes / 8);
+// First tile (per CTA) that takes the per-tile path. Nearly every logit of
+// the first tile passes (the lists are empty), and many of the second at 100+
+// positions (more than the buckets hold): both go through the chunked path.
+#ifndef DFL_LM_FAST_FROM
+#define DFL_LM_FAST_FROM 2
+#endif
+
+// Inserts the keys bk[s * bstride] (s < n) that exceed th into the sorted list
+// l[i * LS] (i < KK, descending) of one position, in registers; th rises to
+// the list's K-th key as it fills. Returns whether the list changed; kth is
+// its K-th key afterwards.
+template <int KK>
+__device__ __forceinline__ bool insert_into_list(uint64_t *l, int LS, const uint64_t *bk, int bstride, int n,
+                                                 uint64_t &th, uint64_t &kth)
+{
+    uint64_t y[KK];
+#pragma unroll
+    for (int i = 0; i < KK; ++i) y[i] = l[i * LS];
+    bool dirty = false;
+    for (int s2 = 0; s2 < n; ++s2) {
+        const uint64_t x = bk[s2 * bstride];
+        if (x <= th) continue;
+        // keys are distinct: the ones below x move down one place
+#pragma unroll
+        for (int i = KK - 1; i > 0; --i) y[i] = y[i - 1] < x ? y[i - 1] : (y[i] < x ? x : y[i]);
+        y[0] = y[0] < x ? x : y[0];
+        th = y[KK - 1] > th ? y[KK - 1] : th;
+        dirty = true;
+    }
+    if (dirty) {
+#pragma unroll
+        for (int i = 0; i < KK; ++i) l[i * LS] = y[i];
+    }
+    kth = y[KK - 1];
+    return dirty;
+}
+
+// Bitonic sort of one 32-bit value per lane, descending (lane 0 largest).
+__device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t x, int lane)
+{
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int jm = k >> 1; jm > 0; jm >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, x, jm);
+            const bool keep_max = ((lane & jm) == 0) == ((lane & k) == 0);
+            x = keep_max ? (x > o ? x : o) : (x < o ? x : o);
+        }
+    }
+    return x;
+}
+
+// v[jj] for a runtime jj in [0, 16), by a select tree on the bits of jj (an
+// indexed read would move the register array to local memory).
+__device__ __forceinline__ float pick16(const float (&v)[16], int jj)
+{
+    float a[8], b[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (jj & 1) ? v[2 * i + 1] : v[2 * i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = (jj & 2) ? a[2 * i + 1] : a[2 * i];
+    const float c0 = (jj & 4) ? b[1] : b[0], c1 = (jj & 4) ? b[3] : b[2];
+    return (jj & 8) ? c1 : c0;
+}
 
 __device__ __forceinline__ void named_bar_sync(int id, int n)
 {
@@ -68,15 +136,30 @@ __host__ __device__ inline int acc_chains(int NT)
 #endif
 }
 
+// Accumulator buffers in TMEM: four where they fit in the 512 columns, so that
+// the MMAs can run up to three tiles ahead of the epilogue (the first tiles of
+// a CTA, whose lists start empty, take the epilogue longer than a tile of the
+// weight stream), else two.
+__host__ __device__ inline int acc_buffers(int NT)
+{
+#ifdef DFL_LM_ACC_BUFS
+    const int want = DFL_LM_ACC_BUFS;
+#else
+    const int want = 4;
+#endif
+    return want * acc_chains(NT) * NT <= 512 ? want : 2;
+}
+
 __host__ __device__ inline uint32_t tmem_cols_for(int NT)
 {
-    uint32_t need = 2u * static_cast<uint32_t>(acc_chains(NT) * NT), c = 32;
+    uint32_t need = static_cast<uint32_t>(acc_buffers(NT) * acc_chains(NT) * NT), c = 32;
     while (c < need) c <<= 1;
     return c;
 }
 
 struct Layout {
-    uint32_t stage_bytes, off_T, off_wscr, off_list, off_thr, off_thrf, off_rb, off_flags, off_cmask, off_bar, total;
+    uint32_t stage_bytes, off_T, off_wscr, off_list, off_thr, off_thrf, off_rb, off_flags, off_cmask, off_ccnt, off_bar,
+        total;
 };
 
 __host__ __device__ inline Layout make_layout(int NT, int K, int stages, int boxes)
@@ -86,14 +169,17 @@ __host__ __device__ inline Layout make_layout(int NT, int K, int stages, int box
     l.off_T = stages * l.stage_bytes;
     l.off_wscr = l.off_T + kTransposeBytes;
     l.off_list = l.off_wscr + 8 * kLmTileM;  // eight epilogue warps x 128 row indices
-    l.off_thr = l.off_list + static_cast<uint32_t>(NT) * K * 8;
+    // lists: entry i of position c at [i * (NT + 1) + c] (odd row length: a warp
+    // reading one list and a thread per position both avoid bank conflicts)
+    l.off_thr = l.off_list + static_cast<uint32_t>(NT + 1) * K * 8;
     l.off_thrf = l.off_thr + static_cast<uint32_t>(NT) * 8;
     l.off_rb = l.off_thrf + static_cast<uint32_t>(NT) * 4;
     l.off_flags = l.off_rb + static_cast<uint32_t>(NT) * 8;
-    l.off_cmask = l.off_flags + 16;
-    l.off_bar = l.off_cmask + 16 * 4 * 4;
-    // full[S], empty[S], tfull[2], tempty[2], drain, then tmem base + abort flag
-    l.total = l.off_bar + 8u * (2u * stages + 5u) + 16u;
+    l.off_cmask = l.off_flags + 32;  // flag words 0..2, overflow flags 4..5
+    l.off_ccnt = l.off_cmask + 16 * 4 * 4;
+    l.off_bar = l.off_ccnt + static_cast<uint32_t>(NT) * 4;
+    // full[S], empty[S], tfull[4], tempty[4], drain, then tmem base + abort flag
+    l.total = l.off_bar + 8u * (2u * stages + 9u) + 16u;
     return l;
 }
 
@@ -121,12 +207,17 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     // per column of the current chunk and TMEM lane quadrant: the tile rows whose
     // logit passes the column's float threshold
     uint32_t *const cmask = reinterpret_cast<uint32_t *>(gbase + lay.off_cmask);
+    // per-tile path: survivor keys by position (key s of position c at [s * NT + c],
+    // over the transpose buffer), their counts, and an overflow flag per tile parity
+    uint64_t *const bucket = reinterpret_cast<uint64_t *>(T);
+    uint32_t *const col_cnt = reinterpret_cast<uint32_t *>(gbase + lay.off_ccnt);
+    volatile uint32_t *const ovf = chunk_flags + 4;
     const uint32_t bar_full = base + lay.off_bar;
     const uint32_t bar_empty = bar_full + 8u * S;
     const uint32_t bar_tfull = bar_empty + 8u * S;
-    const uint32_t bar_tempty = bar_tfull + 16u;
-    const uint32_t bar_drain = bar_tempty + 16u;
-    uint32_t *const tmem_holder = reinterpret_cast<uint32_t *>(gbase + lay.off_bar + 8u * (2u * S + 5u));
+    const uint32_t bar_tempty = bar_tfull + 32u;
+    const uint32_t bar_drain = bar_tempty + 32u;
+    uint32_t *const tmem_holder = reinterpret_cast<uint32_t *>(gbase + lay.off_bar + 8u * (2u * S + 9u));
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,13 +227,14 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     const int KB = p.d / (kLmTileK * BX);
     const uint32_t tmem_cols = tmem_cols_for(NT);
     const int C = acc_chains(NT);
+    const int NA = acc_buffers(NT);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(bar_full + 8u * s, 1);
             mbar_init(bar_empty + 8u * s, 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < 4; ++a) {
             mbar_init(bar_tfull + 8u * a, 1);
             mbar_init(bar_tempty + 8u * a, 128);
         }
@@ -150,12 +242,14 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         *abort_flag = 0;
         fence_mbar_init();
     }
-    for (int i = threadIdx.x; i < NT * K; i += kLmThreads) lists[i] = 0;
+    const int LS = NT + 1;  // row length of the lists
+    for (int i = threadIdx.x; i < LS * K; i += kLmThreads) lists[i] = 0;
+    for (int i = threadIdx.x; i < NT; i += kLmThreads) col_cnt[i] = 0;
     for (int i = threadIdx.x; i < NT; i += kLmThreads) {
         thr[i] = 0;
         thr_f[i] = -INFINITY;
     }
-    if (threadIdx.x < 4) chunk_flags[threadIdx.x] = 0;
+    if (threadIdx.x < 8) chunk_flags[threadIdx.x] = 0;
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.tm_w);
         tma_prefetch_desc(&p.tm_gate);
@@ -239,8 +333,8 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
             int it = 0, j = 0;
             bool ok = true;
             for (int m = chunk; ok && m < p.m_tiles_total; m += G, ++j) {
-                const int a = j & 1;
-                const uint32_t u = static_cast<uint32_t>(j >> 1);
+                const int a = j % NA;
+                const uint32_t u = static_cast<uint32_t>(j / NA);
                 if (!mbar_wait(bar_tempty + 8u * a, (u & 1u) ^ 1u, abort_flag)) {
                     ok = false;
                     break;
@@ -293,9 +387,12 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         int nchunk = 0;  // top-K chunks processed so far (selects the flag word)
         bool ok = true;
         for (int m = chunk; m < p.m_tiles_total; m += G, ++j) {
-            const int a = j & 1;
-            const uint32_t u = static_cast<uint32_t>(j >> 1);
+            const int a = j % NA;
+            const uint32_t u = static_cast<uint32_t>(j / NA);
             const bool gate = m >= p.m_tiles_vocab;
+            // the overflow flag of the next tile: every thread read it (as the
+            // flag of tile j - 1) before the barriers that ended that tile
+            if (threadIdx.x == 64) ovf[(j + 1) & 1] = 0;
             // the cross-CTA thresholds, fetched while the accumulator fills
             uint64_t tg[2] = {0ull, 0ull};
             if (!gate) {
@@ -327,8 +424,8 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                         const uint32_t o = static_cast<uint32_t>(t[u2]);
                         if (static_cast<uint32_t>(t[u2] >> 32) == p.epoch && o > best) best = o;
                     }
-                    const uint64_t srt = warp_sort_desc(static_cast<uint64_t>(best), lane);
-                    const uint64_t kth = shfl_u64(srt, K - 1);
+                    const uint32_t srt = warp_sort_desc_u32(best, lane);
+                    const uint64_t kth = __shfl_sync(0xFFFFFFFFu, srt, K - 1);
                     if (lane == 0) rb[col] = kth << 32;  // any key of that logit value or above passes
                 }
             }
@@ -355,7 +452,83 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(a * C * NT);
             const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
-            for (int c0 = 0; c0 < ncols16; c0 += 16) {
+            bool released = false;  // the accumulator is handed back to the MMA warp
+            const int capc = kBucketKeys / NT;  // keys per position and tile
+            if (!gate && j >= DFL_LM_FAST_FROM && NT >= 32 && NT <= 128) {
+                // Once the lists are warm few logits pass. All eight warps read
+                // the tile (warps w and w + 4 share a lane quadrant, each takes
+                // every other 16-column chunk), file the survivors by position,
+                // and then one thread per position inserts them into its list:
+                // no per-chunk barriers. A tile with more survivors at a position
+                // than the buckets hold goes through the chunked path below (its
+                // accumulator is still held).
+                {
+                    const bool rowok = static_cast<int64_t>(row0) + row < p.V;
+                    const float4 *const thr4 = reinterpret_cast<const float4 *>(thr_f);
+                    for (int ci = ew >> 2; ci * 16 < ncols16; ci += 2) {
+                        const int c0 = ci * 16;
+                        float v[16];
+                        __syncwarp();
+                        tmem_load16(taddr + static_cast<uint32_t>(c0), v);
+                        for (int c = 1; c < C; ++c) {  // the other chains' partial sums, in chain order
+                            float w[16];
+                            tmem_load16(taddr + static_cast<uint32_t>(c * NT + c0), w);
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) v[jj] += w[jj];
+                        }
+                        const int vcols = nvalid - c0;
+                        uint32_t pm = 0;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const float4 t4 = thr4[(c0 >> 2) + q4];
+                            const float tt[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int jj = q4 * 4 + e;
+                                if (jj < vcols && v[jj] >= tt[e]) pm |= 1u << jj;
+                            }
+                        }
+                        if (!rowok) pm = 0;
+                        while (pm) {  // rare: a few survivors per tile and position
+                            const int jj = __ffs(pm) - 1;
+                            pm &= pm - 1;
+                            const int col = c0 + jj;
+                            const uint32_t slot = atomicAdd(col_cnt + col, 1u);
+                            if (slot < static_cast<uint32_t>(capc))
+                                bucket[slot * NT + col] = make_key(pick16(v, jj), static_cast<uint32_t>(row0 + row));
+                            else
+                                ovf[j & 1] = 1;
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                named_bar_sync(1, 256);
+                int nsurv = 0;
+                if (et < nvalid) {
+                    nsurv = static_cast<int>(col_cnt[et]);
+                    col_cnt[et] = 0;  // only this thread touches it until the next tile's filter
+                }
+                if (ovf[j & 1] == 0) {  // uniform: all read the same flag
+                    released = true;
+                    if (tmem_warp) mbar_arrive(bar_tempty + 8u * a);
+                    if (nsurv > 0) {  // thread et owns position et
+                        const int c = et;
+                        uint64_t th = thr[c], kth = 0;
+                        const bool dirty =
+                            K == 16 ? insert_into_list<16>(lists + c, LS, bucket + c, NT, nsurv, th, kth)
+                                    : insert_into_list<32>(lists + c, LS, bucket + c, NT, nsurv, th, kth);
+                        if (dirty) {
+                            thr[c] = th;
+                            thr_f[c] = th ? key_val(th) : -INFINITY;
+                            if (kth) atomicMax(reinterpret_cast<unsigned long long *>(p.thr_g + col_base + c),
+                                               static_cast<unsigned long long>(kth));
+                        }
+                    }
+                    named_bar_sync(1, 256);  // lists and thresholds complete for the next tile
+                }
+            }
+            // the chunked path: the first tile(s), W_H tiles and overflowing tiles
+            for (int c0 = 0; !released && c0 < ncols16; c0 += 16) {
                 float v[16];
                 if (tmem_warp) {
                     __syncwarp();
@@ -423,7 +596,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     }
                     const bool loaded = total > 0;
                     uint64_t mine = 0;
-                    if (loaded) mine = (lane < K) ? lists[col * K + lane] : 0ull;
+                    if (loaded) mine = (lane < K) ? lists[lane * LS + col] : 0ull;
                     if (total > kInsertLimit) {
                         // many survivors (early tiles): pack their tile rows densely
                         // in this warp's scratch, then rebuild, sort 32 at a time
@@ -437,9 +610,36 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                             base_i += __popc(surv[qq]);
                         }
                         __syncwarp();
-                        for (int b0 = 0; b0 < total; b0 += 32) {
+                        int nsort = total;
+                        if (total > 64) {
+                            // The K-th largest of the lanes' maxima (lane l takes
+                            // entries l, l + 32, ...) bounds the K-th best of these
+                            // logits from below: K lanes hold one at least that
+                            // large. The rows below it are dropped before sorting.
+                            float lm = -INFINITY;
+                            for (int e = lane; e < total; e += 32) lm = fmaxf(lm, T[cc * kLmTileM + scr[e]]);
+                            const uint32_t srt = warp_sort_desc_u32(f32_to_ordered(lm), lane);
+                            const float bound = ordered_to_f32(__shfl_sync(0xFFFFFFFFu, srt, K - 1));
+                            int out = 0;  // compacted in place: writes never pass the entries still to be read
+                            for (int e0 = 0; e0 < total; e0 += 32) {
+                                const int e = e0 + lane;
+                                int r = 0;
+                                bool keep = false;
+                                if (e < total) {
+                                    r = scr[e];
+                                    keep = T[cc * kLmTileM + r] >= bound;
+                                }
+                                const unsigned kb = __ballot_sync(0xFFFFFFFFu, keep);
+                                __syncwarp();
+                                if (keep) scr[out + __popc(kb & lt)] = static_cast<uint8_t>(r);
+                                out += __popc(kb);
+                                __syncwarp();
+                            }
+                            nsort = out;
+                        }
+                        for (int b0 = 0; b0 < nsort; b0 += 32) {
                             uint64_t x = 0ull;
-                            if (b0 + lane < total) {
+                            if (b0 + lane < nsort) {
                                 const int r = scr[b0 + lane];
                                 x = make_key(T[cc * kLmTileM + r], static_cast<uint32_t>(row0 + r));
                             }
@@ -466,7 +666,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                         }
                     }
                     if (loaded) {
-                        if (lane < K) lists[col * K + lane] = mine;
+                        if (lane < K) lists[lane * LS + col] = mine;
                         const uint64_t kth = shfl_u64(mine, K - 1);
                         if (lane == 0) {
                             thr[col] = th;
@@ -479,7 +679,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                 }
                 named_bar_sync(1, 256);
             }
-            if (tmem_warp) {
+            if (tmem_warp && !released) {
                 tc_fence_before_sync();
                 mbar_arrive(bar_tempty + 8u * a);
             }
@@ -490,7 +690,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     const int c = et + h * 256;
                     if (c < nvalid)
                         p.tmax[static_cast<size_t>(chunk) * p.N + col_base + c] =
-                            (static_cast<uint64_t>(p.epoch) << 32) | (lists[c * K] >> 32);
+                            (static_cast<uint64_t>(p.epoch) << 32) | (lists[c] >> 32);
                 }
             }
         }
@@ -498,7 +698,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         named_bar_sync(1, 256);
         for (int i = et; i < nvalid * K; i += 256) {
             const int col = i / K;
-            p.part[(static_cast<size_t>(chunk) * p.N + col_base + col) * K + (i % K)] = lists[i];
+            p.part[(static_cast<size_t>(chunk) * p.N + col_base + col) * K + (i % K)] = lists[(i % K) * LS + col];
         }
     }
 
