@@ -372,13 +372,14 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         }
     } else {
         // ------------------------------------------------ epilogue
-        // Warps 2..5 read TMEM (warp w may only touch lane quadrant w % 4);
-        // warps 6..9 only help with the per-position list work. All eight
-        // meet at named barrier 1.
+        // Warps 2..5 read TMEM in the chunked path and release each
+        // accumulator (warp w may only touch lane quadrant w % 4); in the
+        // per-tile path warps 6..9 read it too, from the same quadrants. All
+        // eight share the per-position list work and meet at named barrier 1.
         const bool tmem_warp = warp < 6;
         const int ew = warp - 2;           // 0..7: column share
-        const int q = warp & 3;            // TMEM lane quadrant (TMEM warps)
-        const int row = q * 32 + lane;     // tile row owned by this thread (TMEM warps)
+        const int q = warp & 3;            // TMEM lane quadrant
+        const int row = q * 32 + lane;     // tile row owned by this thread when it reads TMEM
         const int et = threadIdx.x - 64;   // 0..255 among the epilogue threads
         const int col_base = n_tile * NT;
         const int nvalid = min(NT, p.N - col_base);
