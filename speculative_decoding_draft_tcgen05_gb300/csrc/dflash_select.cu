@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -143,6 +144,8 @@ struct dflash_select_ctx {
     float *tab = nullptr;  // [V][512] precomputed A|B of every token (cfg.tables)
     int32_t *ids = nullptr;
     unsigned *ticket = nullptr;
+    float *proj_part = nullptr;     // [2][rows][512] partial sums of the split projection
+    unsigned *proj_ticket = nullptr;
     int *err = nullptr;
     // staging of dflash_select_step_host
     uint16_t *st_hidden = nullptr;
@@ -229,6 +232,9 @@ static dflash_status build_tables(dflash_select_ctx *c, cudaStream_t s)
     pp.K = c->cfg.K;
     pp.R = 1;
     pp.R_total = static_cast<int>(V);
+    pp.ksplit = 1;
+    pp.part = nullptr;
+    pp.ticket = nullptr;
     if (e == cudaSuccess) e = dfl::launch_projection(pp, nc, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     cudaFree(rows);
@@ -333,6 +339,11 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     const size_t o_AB = off; off += up(Bm * c->R * 512 * 4);
     const size_t o_P = off; off += up(Nmax * cfg->K * cfg->K * 4);
     const size_t o_ticket = off; off += up(Bm * 4);
+    // the projection's split along d applies up to projection_split_rows rows
+    const size_t split_rows =
+        std::min(static_cast<size_t>(dfl::projection_split_rows(prop.multiProcessorCount)), Bm * c->R);
+    const size_t o_ppart = off; off += up(2 * split_rows * 512 * 4);
+    const size_t o_ptick = off; off += up(static_cast<size_t>(8 * (prop.multiProcessorCount / 16 + 1)) * 4);
     const size_t o_err = off; off += up(4);
     const size_t o_hid = off; off += up(Nmax * cfg->d * 2);
     const size_t o_anc = off; off += up(Bm * 4);
@@ -361,6 +372,8 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     c->AB = reinterpret_cast<float *>(w + o_AB);
     c->P = reinterpret_cast<float *>(w + o_P);
     c->ticket = reinterpret_cast<unsigned *>(w + o_ticket);
+    c->proj_part = reinterpret_cast<float *>(w + o_ppart);
+    c->proj_ticket = reinterpret_cast<unsigned *>(w + o_ptick);
     c->err = reinterpret_cast<int *>(w + o_err);
     c->st_hidden = reinterpret_cast<uint16_t *>(w + o_hid);
     c->st_anchor = reinterpret_cast<int32_t *>(w + o_anc);
@@ -524,6 +537,9 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
     pp.K = c->cfg.K;
     pp.R = c->R;
     pp.R_total = pl.R_total;
+    pp.ksplit = dfl::projection_ksplit(pl.R_total, nc, c->cfg.d, c->num_sms);
+    pp.part = c->proj_part;
+    pp.ticket = c->proj_ticket;
     if (!c->tab) {
         prof_begin(c, 2, s);
         CUDA_TRY(dfl::launch_projection(pp, nc, s));

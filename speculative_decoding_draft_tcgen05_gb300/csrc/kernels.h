@@ -105,11 +105,18 @@ struct ProjParams {
     int *err;
     int64_t V;
     int d, L, K, R, R_total;      // gathered row gr: sequence gr / R, row gr % R (0: x0, else a candidate)
+    int ksplit;                   // CTAs per output tile along d (1 or 2)
+    float *part;                  // [ksplit][R_total][512] partial sums (ksplit > 1)
+    unsigned *ticket;             // [row tiles][512 / NC] zero on entry, left zero (ksplit > 1)
 };
 cudaError_t prepare_projection(int smem_optin);
 // Output columns per CTA (64, 128 or 256) for R_total gathered rows: the
 // narrowest whose grid still fits one CTA per SM.
 int projection_cols(int R_total, int num_sms);
+// CTAs per output tile along d for R_total rows and NC output columns (1 or 2),
+// and the most rows for which it can be 2 (the partial-sum workspace's size).
+int projection_ksplit(int R_total, int NC, int d, int num_sms);
+int projection_split_rows(int num_sms);
 // p.tm_wa / p.tm_wb must have boxes of 64 columns x NC rows.
 cudaError_t launch_projection(const ProjParams &p, int NC, cudaStream_t s);
 

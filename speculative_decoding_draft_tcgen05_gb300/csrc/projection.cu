@@ -21,6 +21,11 @@
 // Warp roles: warp 0 lane 0 TMA, warp 1 TMEM owner and MMA issuer, warps 2-9
 // gather, then warps 2-5 move the accumulator from TMEM to global memory.
 // Every pipeline wait is bounded.
+//
+// With few rows (a grid that would fill at most half the SMs) d is split in
+// two: CTA z of a tile streams the z-th half of d and writes a partial sum;
+// the tile's second CTA to finish (an atomic ticket, no waiting) adds the two
+// halves in order and writes A|B, so results do not depend on timing.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -69,8 +74,8 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// grid (512 / NC output tiles, ceil(R_total / 128) row tiles), 320 threads.
-// p.tm_wa / p.tm_wb have boxes of 64 columns x NC rows.
+// grid (512 / NC output tiles, ceil(R_total / 128) row tiles, p.ksplit), 320
+// threads. p.tm_wa / p.tm_wb have boxes of 64 columns x NC rows.
 template <int NC>
 __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __grid_constant__ ProjParams p)
 {
@@ -96,7 +101,11 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
     const int wrow0 = (ct % (256 / NC)) * NC;  // first weight row of this tile
     const int row0 = blockIdx.y * kPrRows;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int KB = p.d / 64;
+    // this CTA's k-blocks of 64 columns: [kb0, kb0 + KB)
+    const int KB_all = p.d / 64;
+    const int KB_per = (KB_all + p.ksplit - 1) / p.ksplit;
+    const int kb0 = static_cast<int>(blockIdx.z) * KB_per;
+    const int KB = min(KB_all, kb0 + KB_per) - kb0;
     const CUtensorMap *const tmw = half ? &p.tm_wb : &p.tm_wa;
 
     if (threadIdx.x == 0) {
@@ -128,7 +137,7 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
             const int pre = KB < kPrStages ? KB : kPrStages;
             for (int kb = 0; kb < pre; ++kb) {  // weights: before the dependency wait
                 mbar_arrive_expect_tx(bar_full + 8u * kb, kPrWBytes);
-                tma_load_2d(base + kb * kPrStageBytes + kPrEBytes, tmw, kb * 64, wrow0, bar_full + 8u * kb, pol);
+                tma_load_2d(base + kb * kPrStageBytes + kPrEBytes, tmw, (kb0 + kb) * 64, wrow0, bar_full + 8u * kb, pol);
             }
             int kb = pre;
             for (; kb < KB; ++kb) {
@@ -138,7 +147,7 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
                     break;
                 }
                 mbar_arrive_expect_tx(bar_full + 8u * s, kPrWBytes);
-                tma_load_2d(base + s * kPrStageBytes + kPrEBytes, tmw, kb * 64, wrow0, bar_full + 8u * s, pol);
+                tma_load_2d(base + s * kPrStageBytes + kPrEBytes, tmw, (kb0 + kb) * 64, wrow0, bar_full + 8u * s, pol);
             }
             if (timed_out)  // let the copies already issued land before the CTA can exit
                 for (int j = (kb > kPrStages ? kb - kPrStages : 0); j < kb; ++j)
@@ -197,7 +206,7 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
                 const int i = gt + u * kPrGather;
                 const int r = i >> 3, c = i & 7;
                 const int32_t t = tok[r];
-                const uint16_t *src = p.E + static_cast<size_t>(t < 0 ? 0 : t) * p.d + kb * 64 + c * 8;
+                const uint16_t *src = p.E + static_cast<size_t>(t < 0 ? 0 : t) * p.d + (kb0 + kb) * 64 + c * 8;
                 cp_async16(et + swz128(r, c), src, t < 0 ? 0u : 16u);  // rows past the end read as zero
             }
             cp_async_commit();
@@ -223,7 +232,8 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
         const int r = q * 32 + lane;
         const int gr = row0 + r;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        float *const dst = p.AB + static_cast<size_t>(gr < p.R_total ? gr : 0) * 512 + ct * NC;
+        float *const out = p.ksplit > 1 ? p.part + static_cast<size_t>(blockIdx.z) * p.R_total * 512 : p.AB;
+        float *const dst = out + static_cast<size_t>(gr < p.R_total ? gr : 0) * 512 + ct * NC;
         for (int c0 = 0; c0 < NC; c0 += 16) {
             float v[16];
             __syncwarp();
@@ -241,6 +251,37 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, NC);
+    }
+    if (p.ksplit > 1) {
+        // the tile's last CTA adds the partial sums in split order
+        __shared__ int last;
+        __threadfence();  // this thread's partial sums before the ticket
+        __syncthreads();
+        unsigned *const tk = p.ticket + blockIdx.y * gridDim.x + blockIdx.x;
+        if (threadIdx.x == 0) {
+            last = atomicAdd(tk, 1u) == static_cast<unsigned>(p.ksplit - 1);
+            if (last) *tk = 0;  // ready for the next run
+        }
+        __syncthreads();
+        if (last) {
+            __threadfence();
+            constexpr int nc4 = NC / 4;
+            const size_t zstride = static_cast<size_t>(p.R_total) * 512;
+            for (int e = threadIdx.x; e < kPrRows * nc4; e += kPrThreads) {
+                const int gr = row0 + e / nc4;
+                if (gr >= p.R_total) break;  // e grows with the row
+                const size_t off = static_cast<size_t>(gr) * 512 + ct * NC + (e % nc4) * 4;
+                float4 acc = __ldcg(reinterpret_cast<const float4 *>(p.part + off));
+                for (int z = 1; z < p.ksplit; ++z) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part + z * zstride + off));
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
+                }
+                *reinterpret_cast<float4 *>(p.AB + off) = acc;
+            }
+        }
     }
 }
 
@@ -262,6 +303,18 @@ cudaError_t prepare_projection(int smem_optin)
     return e;
 }
 
+int projection_ksplit(int R_total, int NC, int d, int num_sms)
+{
+    const int rt = (R_total + kPrRows - 1) / kPrRows;
+    return (2 * (512 / NC) * rt <= num_sms && d / 64 >= 8) ? 2 : 1;
+}
+
+int projection_split_rows(int num_sms)
+{
+    // the split needs 2 x 8 CTAs per row tile (64 output columns: the narrowest tiles)
+    return (num_sms / 16) * kPrRows;
+}
+
 int projection_cols(int R_total, int num_sms)
 {
     const int rt = (R_total + kPrRows - 1) / kPrRows;
@@ -272,7 +325,7 @@ int projection_cols(int R_total, int num_sms)
 
 cudaError_t launch_projection(const ProjParams &p, int NC, cudaStream_t s)
 {
-    const dim3 grid(512 / NC, (p.R_total + kPrRows - 1) / kPrRows);
+    const dim3 grid(512 / NC, (p.R_total + kPrRows - 1) / kPrRows, p.ksplit);
     if (NC == 64) return launch_ex(projection_tc_kernel<64>, grid, dim3(kPrThreads), PrShape<64>::kSmem, s, 1, p);
     if (NC == 128) return launch_ex(projection_tc_kernel<128>, grid, dim3(kPrThreads), PrShape<128>::kSmem, s, 1, p);
     return launch_ex(projection_tc_kernel<256>, grid, dim3(kPrThreads), PrShape<256>::kSmem, s, 1, p);
