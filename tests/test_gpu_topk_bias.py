@@ -50,6 +50,9 @@ CASES = [
     (wl.custom(name="rising_b32", B=32, L=7, K=16, V=65536, d=128, seed=31, std_w=0.05), 0.022),
     # 56 positions: one position tile of 64, buckets of 16 keys per position
     (wl.custom(name="rising_b8", B=8, L=7, K=16, V=65536, d=128, seed=32, std_w=0.05), 0.012),
+    # K = 32 on a 32-wide position tile (buckets of 32 keys): the per-tile path's
+    # 32-entry insertion; V = 50000 gives 89 CTAs a third tile
+    (wl.custom(name="rising_k32", B=4, L=8, K=32, V=50000, d=128, seed=33, std_w=0.05), 0.012),
 ]
 
 
