@@ -205,8 +205,9 @@ int32_t dflash_select_launches_per_run(dflash_select_handle h, int32_t B);
  *   device_status [1] int32 on the device (NULL = not wanted): 0, or the
  *             device error bits (2 = a pipeline wait ran out of time)
  * Limits: 1 <= N <= 256, K in {16, 32}, d % 64 == 0, and the partial lists
- * (min(SMs, ceil(V / 128)) * N * K * 8 bytes) must fit in the scratch; larger
- * shapes return DFLASH_ERR_UNSUPPORTED with the sizes in the message.
+ * (min(SMs / T, ceil(V / 128)) * N * K * 8 bytes, with T = ceil(N / 128)
+ * position tiles) must fit in the scratch; larger shapes return
+ * DFLASH_ERR_UNSUPPORTED with the sizes in the message.
  * The first call on a device looks up the scratch's address and sets kernel
  * attributes for that device; make that first call before any stream capture.
  * Every call on a device shares the one scratch array, which keeps the last

@@ -115,9 +115,15 @@ extern "C" dflash_status dflash_lmhead_topk_noalloc(const void *W_lm, int64_t V,
     dflash_status st = setup_current_device(&dev);
     if (st != DFLASH_OK) return st;
 
-    const int NT = ((N + 15) / 16) * 16;
+    // The selector's own tiling for up to 256 positions: position tiles of at
+    // most 128 (the per-tile epilogue's range), each with its own share of the
+    // SMs.
+    const int n_tiles_n = (N + 127) / 128;
+    const int NT = ((N + n_tiles_n - 1) / n_tiles_n + 15) / 16 * 16;
     const int m_tiles = static_cast<int>((V + dfl::kLmTileM - 1) / dfl::kLmTileM);
-    const int G = dev.num_sms < m_tiles ? dev.num_sms : m_tiles;
+    int G = dev.num_sms / n_tiles_n;
+    if (G < 1) G = 1;
+    if (G > m_tiles) G = m_tiles;
     const size_t part_bytes = static_cast<size_t>(G) * N * K * sizeof(uint64_t);
     if (part_bytes > kPartBytes)
         return fail(DFLASH_ERR_UNSUPPORTED,
@@ -132,7 +138,7 @@ extern "C" dflash_status dflash_lmhead_topk_noalloc(const void *W_lm, int64_t V,
     p.d = d;
     p.N = N;
     p.NT = NT;
-    p.n_tiles_n = 1;
+    p.n_tiles_n = n_tiles_n;
     p.K = K;
     p.m_tiles_vocab = m_tiles;
     p.m_tiles_total = m_tiles;
@@ -155,7 +161,7 @@ extern "C" dflash_status dflash_lmhead_topk_noalloc(const void *W_lm, int64_t V,
     // the error word and the per-position thresholds must start at zero
     if (cudaMemsetAsync(dev.scratch, 0, kZeroBytes, s) != cudaSuccess)
         return fail(DFLASH_ERR_CUDA, "clearing the scratch failed");
-    cudaError_t e = dfl::launch_lmhead_topk(p, G, dfl::lmhead_smem_bytes(NT, K, stages, p.boxes), s);
+    cudaError_t e = dfl::launch_lmhead_topk(p, G * n_tiles_n, dfl::lmhead_smem_bytes(NT, K, stages, p.boxes), s);
     if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "lm_head kernel launch failed (error %lld)", e);
     float *vals = topk_vals ? topk_vals : reinterpret_cast<float *>(dev.scratch + kValsOffset);
     e = dfl::launch_topk_merge(p.part, G, N, K, topk_ids, vals, nullptr, nullptr, p.thr_g, s);

@@ -306,7 +306,11 @@ cudaError_t prepare_projection(int smem_optin)
 int projection_ksplit(int R_total, int NC, int d, int num_sms)
 {
     const int rt = (R_total + kPrRows - 1) / kPrRows;
-    return (2 * (512 / NC) * rt <= num_sms && d / 64 >= 8) ? 2 : 1;
+    // halves of equal length only: an odd count of 64-column blocks keeps one
+    // CTA per tile (with d a multiple of 64 but not of 128 the small-batch
+    // tail runs clusters of one CTA, so the three-kernel tail, the only user of
+    // the split, never sees so few rows there anyway)
+    return (2 * (512 / NC) * rt <= num_sms && d / 64 >= 8 && (d / 64) % 2 == 0) ? 2 : 1;
 }
 
 int projection_split_rows(int num_sms)

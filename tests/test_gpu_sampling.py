@@ -44,7 +44,10 @@ def _gpu_sampled(pkg, inp, hidden, anchor, u_walk, T):
         pkg.dflash_select_run_sampled(sel.h, hidden.cuda(), anchor.cuda(), torch.from_numpy(u_walk).cuda(), **out)
         pkg.dflash_select_sync_status(sel.h)
         torch.cuda.synchronize()
-    return {k: v.cpu().numpy() for k, v in out.items()}
+        launches = pkg.dflash_select_launches_per_run(sel.h, B)
+    res = {k: v.cpu().numpy() for k, v in out.items()}
+    res["fused_tail"] = launches == 2  # lm_head + the clustered tail; else merge, projection, pair tables + walk
+    return res
 
 
 def _target_probs(rng, q_rows, ids_rows, V, L):
@@ -61,23 +64,33 @@ def _target_probs(rng, q_rows, ids_rows, V, L):
 
 def _check_walk(inp, gpu, seqs_hidden_idx, u_walk, T):
     """Per replica b (hidden of sequence seqs_hidden_idx[b]): the GPU's sampled
-    path and draft distribution against the oracle's."""
+    path and draft distribution against the oracle's sampling walk over the
+    oracle's tables on the GPU's (validated) candidate sets; the draws whose
+    uniform lies within SAMPLE_EPS of a CDF boundary are excused, and so is
+    the rest of the walk after them."""
     w = inp.wl
     orc = parity.run_oracle(inp, sorted(set(seqs_hidden_idx)))
-    rep = dict(checked=0, excused=0)
+    rep = dict(checked=0, excused=0, steps_checked=0, flags_checked=0)
     for b, s in enumerate(seqs_hidden_idx):
-        r = orc[s]
-        ranks, q, mg = oracle.sample_walk(r["P"], T, u_walk[b].astype(np.float64))
-        tokens = r["ids"][np.arange(w.L), ranks]
-        if (r["topk_margin"] < parity.TIE_EPS).any() or (mg < SAMPLE_EPS).any():
-            rep["excused"] += 1
-            continue
-        assert gpu["path"][b].tolist() == tokens.tolist(), f"replica {b}: sampled path"
-        for t in range(w.L):
-            by_id = dict(zip(r["ids"][t].tolist(), q[t].tolist()))
+        c, _ = parity.conditional_reference(inp, s, orc[s], gpu["topk_ids"][b])
+        ranks, q, mg = oracle.sample_walk(c["P"], T, u_walk[b].astype(np.float64))
+        tokens = c["ids"][np.arange(w.L), ranks]
+        open_at = [t for t in range(w.L) if mg[t] < SAMPLE_EPS]
+        decided = open_at[0] if open_at else w.L
+        assert gpu["path"][b][:decided].tolist() == tokens[:decided].tolist(), f"replica {b}: sampled path"
+        for t in range(decided + 1 if decided < w.L else w.L):  # the distribution at the first open step is known
+            by_id = dict(zip(c["ids"][t].tolist(), q[t].tolist()))
             for j, tok in enumerate(gpu["topk_ids"][b][t].tolist()):
                 assert parity.close(gpu["draft_probs"][b][t][j], by_id[tok]), f"replica {b} t {t}: draft prob"
-        rep["checked"] += 1
+        for t in range(decided):  # the flag marks a uniform within tie_eps of a CDF boundary
+            if abs(mg[t] - parity.TIE_EPS) > SAMPLE_EPS:
+                assert bool(gpu["tie_flags"][b][t] & 1) == (mg[t] < parity.TIE_EPS), f"replica {b} t {t}: flag"
+                rep["flags_checked"] += 1
+        rep["steps_checked"] += decided
+        if decided == w.L:
+            rep["checked"] += 1
+        else:
+            rep["excused"] += 1
     return rep, orc
 
 
@@ -94,6 +107,36 @@ def test_sampling_walk_tiny(pkg, T):
     rep, _ = _check_walk(inp, gpu, idx, u_walk, T)
     print("sampling walk tiny T", T, rep)
     assert rep["checked"] >= reps // 2
+
+
+def test_sampling_walk_fused_tail(pkg):
+    """Eight replicas of the tiny workload fit the clustered small-batch tail
+    (the launch configuration of the benchmark's sampling step at batch 1)."""
+    inp = parity.inputs_for("tiny")
+    rng = np.random.default_rng(44)
+    reps = 8
+    idx = [b % inp.wl.B for b in range(reps)]
+    u_walk = rng.random((reps, inp.wl.L)).astype(np.float32)
+    gpu = _gpu_sampled(pkg, inp, inp.hidden[idx].contiguous(), inp.anchor[idx].contiguous(), u_walk, 1.0)
+    assert gpu["fused_tail"]
+    rep, _ = _check_walk(inp, gpu, idx, u_walk, 1.0)
+    print("sampling walk, fused tail", rep)
+    assert rep["checked"] >= reps - 1
+
+
+@pytest.mark.parametrize("reps,fused", [(4, True), (12, False)])
+def test_sampling_walk_k32(pkg, reps, fused):
+    """K = 32 candidates and 16 positions, on both tail paths."""
+    w = wl.custom(name="sample_k32", B=2, L=16, K=32, V=5000, d=192, seed=29, std_w=0.05)
+    inp = wl.make_inputs(w)
+    rng = np.random.default_rng(45 + reps)
+    idx = [b % w.B for b in range(reps)]
+    u_walk = rng.random((reps, w.L)).astype(np.float32)
+    gpu = _gpu_sampled(pkg, inp, inp.hidden[idx].contiguous(), inp.anchor[idx].contiguous(), u_walk, 1.0)
+    assert gpu["fused_tail"] == fused
+    rep, _ = _check_walk(inp, gpu, idx, u_walk, 1.0)
+    print("sampling walk K=32, fused" if fused else "sampling walk K=32, three kernels", rep)
+    assert rep["checked"] >= reps // 2 and rep["steps_checked"] >= 0.75 * reps * w.L
 
 
 def _verify_case(pkg, inp, orc_seq, rng, reps, T):
