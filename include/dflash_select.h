@@ -218,6 +218,54 @@ dflash_status dflash_lmhead_topk_noalloc(const void *W_lm, int64_t V, int32_t d,
                                          int32_t K, int32_t *topk_ids, float *topk_vals, int32_t *device_status,
                                          void *stream);
 
+/* ---- Vocabulary shards (the selector's lm_head split over several GPUs) ----
+ * The top-K of a position over the whole vocabulary is the top-K of the union
+ * of the shards' top-K lists (blog "DFlash 2: Keep Drafting Parallel",
+ * sections "The Right Tokens Are Already There" and "A Lightweight Path
+ * Selector": the K best tokens of the drafter's logit at each position). So a
+ * GPU that holds only the rows [v0, v1) of the lm_head weight can stream them,
+ * keep its own K best per position, and exchange those lists; after the
+ * exchange every GPU merges the G lists and runs the rest of the selector.
+ * A list entry is a 64-bit key: high word = the fp32 logit mapped to an
+ * unsigned integer that preserves its order (bits ^ 0x80000000 for +x, ~bits
+ * for -x, -0 taken as +0), low word = ~token_id; a larger key is a better
+ * candidate (logit descending, then id ascending), and key 0 is below every
+ * real one. */
+
+/* Creates a handle that streams the lm_head rows [v0, v1) only.
+ *   W_shard [v1 - v0, d] bf16  rows v0 .. v1-1 of the lm_head weight
+ *   E, W_A, W_B, W_H           as dflash_select_init (E covers the whole
+ *                              vocabulary: candidates of any shard are gathered)
+ * cfg->V is the whole vocabulary; 0 <= v0 < v1 <= V. Such a handle runs
+ * dflash_select_topk_shard and dflash_select_run_gathered, not
+ * dflash_select_run. Errors: as dflash_select_init. */
+dflash_status dflash_select_init_shard(const dflash_select_config *cfg, const void *W_shard, int64_t v0, int64_t v1,
+                                       const void *E, const void *W_A, const void *W_B, const void *W_H,
+                                       void *stream, dflash_select_handle *out);
+
+/* The handle's shard of the lm_head pass for B sequences: writes the K best
+ * keys of every position over tokens [v0, v1), sorted (best first), into
+ *   shard_keys [B, L, K] uint64 (device)
+ * and keeps g_t = H(h_t) in the handle for dflash_select_run_gathered. Any
+ * handle works (a whole-vocabulary handle is the one-shard case).
+ * Errors: INVALID_ARG, CUDA. */
+dflash_status dflash_select_topk_shard(dflash_select_handle h, const void *hidden, int32_t B, uint64_t *shard_keys,
+                                       void *stream);
+
+/* The rest of the selector after the exchange: merges the G shards' lists
+ *   all_keys [G, B, L, K] uint64 (device; shard g's dflash_select_topk_shard
+ *            output at [g]; the shards' ranges are disjoint and together
+ *            cover [0, V))
+ * into the top-K of every position, then projections, pair tables and the walk,
+ * with the same outputs as dflash_select_run. The gate comes from the last
+ * dflash_select_topk_shard on this handle, which must have run the same batch
+ * earlier on the same stream. Max-sum and greedy walks; 1 <= G <= 1024.
+ * Errors: INVALID_ARG, CUDA. */
+dflash_status dflash_select_run_gathered(dflash_select_handle h, const int32_t *anchor, int32_t B,
+                                         const uint64_t *all_keys, int32_t G, int32_t *topk_ids, float *topk_vals,
+                                         float *pair_scores, int32_t *path, float *path_score, uint8_t *tie_flags,
+                                         void *stream);
+
 /* Frees the workspace (after the device is idle) and the handle. Returns a
  * latched device error if one is pending, else DFLASH_OK. NULL is a no-op. */
 dflash_status dflash_select_destroy(dflash_select_handle h);

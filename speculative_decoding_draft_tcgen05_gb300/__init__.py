@@ -72,6 +72,10 @@ def lib() -> ctypes.CDLL:
             L.dflash_select_launches_per_run.argtypes = [P, i32]
             L.dflash_select_launches_per_run.restype = i32
             L.dflash_select_destroy.argtypes = [P]
+            L.dflash_select_init_shard.argtypes = [ctypes.POINTER(dflash_select_config), P, i64, i64, P, P, P, P, P,
+                                                   ctypes.POINTER(P)]
+            L.dflash_select_topk_shard.argtypes = [P, P, i32, P, P]
+            L.dflash_select_run_gathered.argtypes = [P, P, i32, P, i32, P, P, P, P, P, P, P]
             L.dflash_lmhead_topk_noalloc.argtypes = [P, i64, i32, P, i32, i32, P, P, P, P]
             L.dflash_selftest_wait_timeout.argtypes = [P, P]
             L.dflash_conv2_init.argtypes = [P, P, i32, ctypes.POINTER(P)]
@@ -83,7 +87,8 @@ def lib() -> ctypes.CDLL:
                       "dflash_select_sync_status", "dflash_select_profile", "dflash_select_profile_read",
                       "dflash_select_destroy", "dflash_lmhead_topk_noalloc", "dflash_select_run_sampled",
                       "dflash_verify_rejection", "dflash_conv2_init", "dflash_conv2_run", "dflash_conv2_sync_status",
-                      "dflash_conv2_destroy", "dflash_selftest_wait_timeout"):
+                      "dflash_conv2_destroy", "dflash_selftest_wait_timeout", "dflash_select_init_shard",
+                      "dflash_select_topk_shard", "dflash_select_run_gathered"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -134,6 +139,52 @@ def dflash_select_init(W, E, W_A, W_B, W_H, *, L: int, K: int, max_batch: int, w
                                     _ptr(W_H, torch.bfloat16, "W_H"), _stream(stream), ctypes.byref(h)),
            "dflash_select_init")
     return h
+
+
+def dflash_select_init_shard(W_shard, v0, v1, E, W_A, W_B, W_H, *, L: int, K: int, max_batch: int,
+                             walk: int = DFLASH_WALK_VITERBI, tie_eps: float = 1e-3, tables: bool = False,
+                             stream=None):
+    """A handle that streams the lm_head rows [v0, v1) only: W_shard [v1 - v0, d] holds those rows, E [V, d] the
+    whole token table (V = E's rows)."""
+    import torch
+    V, d = E.shape
+    if tuple(W_shard.shape) != (v1 - v0, d):
+        raise ValueError(f"W_shard must be [{v1 - v0}, {d}], got {tuple(W_shard.shape)}")
+    cfg = dflash_select_config(V=V, d=d, L=L, K=K, e=W_A.shape[0], max_batch=max_batch, walk=walk,
+                               tie_eps=tie_eps, temperature=1.0, tables=1 if tables else 0)
+    h = ctypes.c_void_p()
+    _check(lib().dflash_select_init_shard(ctypes.byref(cfg), _ptr(W_shard, torch.bfloat16, "W_shard"), v0, v1,
+                                          _ptr(E, torch.bfloat16, "E"), _ptr(W_A, torch.bfloat16, "W_A"),
+                                          _ptr(W_B, torch.bfloat16, "W_B"), _ptr(W_H, torch.bfloat16, "W_H"),
+                                          _stream(stream), ctypes.byref(h)), "dflash_select_init_shard")
+    return h
+
+
+def dflash_select_topk_shard(handle, hidden, shard_keys, stream=None):
+    """The handle's vocabulary shard of the lm_head pass: hidden [B, L, d] bf16 into shard_keys [B, L, K] (int64
+    tensor holding the uint64 keys)."""
+    import torch
+    B = hidden.shape[0]
+    _check(lib().dflash_select_topk_shard(handle, _ptr(hidden, torch.bfloat16, "hidden"), B,
+                                          _ptr(shard_keys, torch.int64, "shard_keys"), _stream(stream)),
+           "dflash_select_topk_shard")
+
+
+def dflash_select_run_gathered(handle, anchor, all_keys, *, path, topk_ids=None, topk_vals=None, pair_scores=None,
+                               path_score=None, tie_flags=None, stream=None):
+    """The selector after the exchange: all_keys [G, B, L, K] (int64 tensor of uint64 keys) from every shard."""
+    import torch
+    B = anchor.shape[0]
+    G = all_keys.shape[0]
+    _check(lib().dflash_select_run_gathered(handle, _ptr(anchor, torch.int32, "anchor"), B,
+                                            _ptr(all_keys, torch.int64, "all_keys"), G,
+                                            _ptr(topk_ids, torch.int32, "topk_ids"),
+                                            _ptr(topk_vals, torch.float32, "topk_vals"),
+                                            _ptr(pair_scores, torch.float32, "pair_scores"),
+                                            _ptr(path, torch.int32, "path"),
+                                            _ptr(path_score, torch.float32, "path_score"),
+                                            _ptr(tie_flags, torch.uint8, "tie_flags"), _stream(stream)),
+           "dflash_select_run_gathered")
 
 
 def dflash_select_run(handle, hidden, anchor, *, path, topk_ids=None, topk_vals=None, pair_scores=None,

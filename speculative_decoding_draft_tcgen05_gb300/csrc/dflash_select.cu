@@ -134,6 +134,7 @@ struct dflash_select_ctx {
     const void *h_ptr = nullptr;
     int h_rows = -1;
     int m_tiles_vocab = 0, m_tiles_total = 0, R = 0;
+    int64_t shard_v0 = 0, shard_rows = 0;  // the rows of W_lm this handle streams: tokens [v0, v0 + rows)
 
     void *ws = nullptr;
     uint64_t *part = nullptr;
@@ -264,13 +265,11 @@ static dflash_status check_config(const dflash_select_config *c)
     return ok();
 }
 
-dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_lm, const void *E, const void *W_A,
-                                 const void *W_B, const void *W_H, void *stream, dflash_select_handle *out)
+static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm, int64_t v0, int64_t rows,
+                               const void *E, const void *W_A, const void *W_B, const void *W_H, void *stream,
+                               dflash_select_handle *out)
 {
-    if (!out) return fail(DFLASH_ERR_INVALID_ARG, "out is NULL");
-    *out = nullptr;
-    dflash_status st = check_config(cfg);
-    if (st != DFLASH_OK) return st;
+    dflash_status st;
     const void *ptrs[5] = {W_lm, E, W_A, W_B, W_H};
     const char *names[5] = {"W_lm", "E", "W_A", "W_B", "W_H"};
     for (int i = 0; i < 5; ++i) {
@@ -301,11 +300,13 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     c->device = dev;
     c->num_sms = prop.multiProcessorCount;
     c->smem_optin = prop.sharedMemPerBlockOptin;
-    c->m_tiles_vocab = static_cast<int>((cfg->V + dfl::kLmTileM - 1) / dfl::kLmTileM);
+    c->shard_v0 = v0;
+    c->shard_rows = rows;
+    c->m_tiles_vocab = static_cast<int>((rows + dfl::kLmTileM - 1) / dfl::kLmTileM);
     c->m_tiles_total = c->m_tiles_vocab + dfl::kEmbed / dfl::kLmTileM;
     c->R = cfg->L * cfg->K + 1;
 
-    if ((st = make_tmap(&c->tm_w, W_lm, cfg->V, cfg->d, dfl::kLmTileM)) != DFLASH_OK ||
+    if ((st = make_tmap(&c->tm_w, W_lm, rows, cfg->d, dfl::kLmTileM)) != DFLASH_OK ||
         (st = make_tmap(&c->tm_gate, W_H, dfl::kEmbed, cfg->d, dfl::kLmTileM)) != DFLASH_OK ||
         (st = make_tmap(&c->tm_wa, W_A, dfl::kEmbed, cfg->d, dfl::kEmbed)) != DFLASH_OK ||
         (st = make_tmap(&c->tm_wb, W_B, dfl::kEmbed, cfg->d, dfl::kEmbed)) != DFLASH_OK ||
@@ -404,6 +405,30 @@ dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_
     return ok();
 }
 
+dflash_status dflash_select_init(const dflash_select_config *cfg, const void *W_lm, const void *E, const void *W_A,
+                                 const void *W_B, const void *W_H, void *stream, dflash_select_handle *out)
+{
+    if (!out) return fail(DFLASH_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    dflash_status st = check_config(cfg);
+    if (st != DFLASH_OK) return st;
+    return init_impl(cfg, W_lm, 0, cfg->V, E, W_A, W_B, W_H, stream, out);
+}
+
+dflash_status dflash_select_init_shard(const dflash_select_config *cfg, const void *W_shard, int64_t v0, int64_t v1,
+                                       const void *E, const void *W_A, const void *W_B, const void *W_H, void *stream,
+                                       dflash_select_handle *out)
+{
+    if (!out) return fail(DFLASH_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    dflash_status st = check_config(cfg);
+    if (st != DFLASH_OK) return st;
+    if (v0 < 0 || v1 <= v0 || v1 > cfg->V)
+        return fail(DFLASH_ERR_INVALID_ARG, "the shard [%lld, %lld) must be a non-empty range within [0, V = %lld)",
+                    static_cast<long long>(v0), static_cast<long long>(v1), static_cast<long long>(cfg->V));
+    return init_impl(cfg, W_shard, v0, v1 - v0, E, W_A, W_B, W_H, stream, out);
+}
+
 static void prof_ensure(dflash_select_ctx *c)
 {
     if (!c->ev.empty()) return;
@@ -430,32 +455,22 @@ static void prof_end(dflash_select_ctx *c, int slot, int kid, cudaStream_t s)
     c->prof_rec[c->prof_runs].n = slot + 1;
 }
 
-static dflash_status run_impl(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,
-                              const float *u_walk, int32_t *topk_ids, float *topk_vals, float *pair_scores,
-                              int32_t *path, float *draft_probs, float *path_score, uint8_t *tie_flags,
-                              void *stream)
+// The lm_head + top-K pass (and the gate) of B sequences: partial lists in
+// c->part, g_t in c->gate.
+static dflash_status launch_lmhead(dflash_select_ctx *c, const void *hidden, const Plan &pl, cudaStream_t s)
 {
-    if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
-    dflash_select_ctx *c = h;
-    if (B < 0 || B > c->cfg.max_batch)
-        return fail(DFLASH_ERR_INVALID_ARG, "B must be in [0, max_batch=%d] (got %d)", c->cfg.max_batch, B);
-    if (B == 0) return ok();
-    if (!hidden || !anchor || !path) return fail(DFLASH_ERR_INVALID_ARG, "hidden, anchor and path must not be NULL");
-    if (!aligned16(hidden)) return fail(DFLASH_ERR_INVALID_ARG, "hidden is not 16-byte aligned");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const Plan pl = c->plan(B);
     if (hidden != c->h_ptr || pl.N != c->h_rows) {
         dflash_status st = make_tmap(&c->tm_h, hidden, pl.N, c->cfg.d, pl.NT);
         if (st != DFLASH_OK) return st;
         c->h_ptr = hidden;
         c->h_rows = pl.N;
     }
-
     dfl::LmHeadParams lp;
     lp.tm_w = c->tm_w;
     lp.tm_gate = c->tm_gate;
     lp.tm_h = c->tm_h;
-    lp.V = c->cfg.V;
+    lp.V = c->shard_rows;
+    lp.id_base = static_cast<uint32_t>(c->shard_v0);
     lp.d = c->cfg.d;
     lp.N = pl.N;
     lp.NT = pl.NT;
@@ -477,13 +492,31 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
     prof_begin(c, 0, s);
     CUDA_TRY(dfl::launch_lmhead_topk(lp, pl.grid, pl.smem, s));
     prof_end(c, 0, 0, s);
+    return ok();
+}
 
-    if (pl.fused_tail) {
+// Everything after the lm_head pass: merge of G sorted lists part [G][N][K]
+// (the lm_head CTAs' partial lists, or the vocabulary shards' lists),
+// projections, pair tables and the walk; the gate comes from c->gate.
+static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, int32_t B, const Plan &pl,
+                                 const uint64_t *part, int G, const float *u_walk, int32_t *topk_ids,
+                                 float *topk_vals, float *pair_scores, int32_t *path, float *draft_probs,
+                                 float *path_score, uint8_t *tie_flags, cudaStream_t s)
+{
+    int tail_S = pl.tail_S;
+    size_t tail_smem = pl.tail_smem;
+    bool fused = pl.fused_tail;
+    if (G != pl.G) {
+        tail_S = dfl::tail_stages(c->cfg.K, G, pl.tail_cs, static_cast<int>(c->smem_optin));
+        fused = pl.n_tiles_n == 1 && pl.N * pl.tail_cs <= c->num_sms && tail_S > 0;
+        tail_smem = fused ? dfl::tail_smem_bytes(c->cfg.K, tail_S, G, pl.tail_cs) : 0;
+    }
+    if (fused) {
         dfl::TailParams tp;
         tp.tm_wa = c->tm_wa;
         tp.tm_wb = c->tm_wb;
         tp.tab = c->tab;
-        tp.part = c->part;
+        tp.part = part;
         tp.thr_g = c->thr_g;
         tp.gate = c->gate;
         tp.E = static_cast<const uint16_t *>(c->E);
@@ -502,7 +535,7 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
         tp.V = c->cfg.V;
         tp.d = c->cfg.d;
         tp.L = c->cfg.L;
-        tp.G = pl.G;
+        tp.G = G;
         tp.N = pl.N;
         tp.cs = pl.tail_cs;
         tp.walk = c->cfg.walk;
@@ -511,14 +544,14 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
         tp.q_out = draft_probs;
         tp.temperature = c->cfg.temperature;
         prof_begin(c, 1, s);
-        CUDA_TRY(dfl::launch_select_tail(tp, c->cfg.K, pl.tail_S, pl.tail_smem, s));
+        CUDA_TRY(dfl::launch_select_tail(tp, c->cfg.K, tail_S, tail_smem, s));
         prof_end(c, 1, 4, s);
         if (prof_on(c)) ++c->prof_runs;
         return ok();
     }
 
     prof_begin(c, 1, s);
-    CUDA_TRY(dfl::launch_topk_merge(c->part, pl.G, pl.N, c->cfg.K, c->ids, c->vals, topk_ids, topk_vals, c->thr_g, s));
+    CUDA_TRY(dfl::launch_topk_merge(part, G, pl.N, c->cfg.K, c->ids, c->vals, topk_ids, topk_vals, c->thr_g, s));
     prof_end(c, 1, 1, s);
 
     dfl::ProjParams pp;
@@ -576,6 +609,74 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
     prof_end(c, slot, 3, s);
     if (prof_on(c)) ++c->prof_runs;
     return ok();
+}
+
+static dflash_status run_impl(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,
+                              const float *u_walk, int32_t *topk_ids, float *topk_vals, float *pair_scores,
+                              int32_t *path, float *draft_probs, float *path_score, uint8_t *tie_flags,
+                              void *stream)
+{
+    if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+    dflash_select_ctx *c = h;
+    if (B < 0 || B > c->cfg.max_batch)
+        return fail(DFLASH_ERR_INVALID_ARG, "B must be in [0, max_batch=%d] (got %d)", c->cfg.max_batch, B);
+    if (B == 0) return ok();
+    if (!hidden || !anchor || !path) return fail(DFLASH_ERR_INVALID_ARG, "hidden, anchor and path must not be NULL");
+    if (!aligned16(hidden)) return fail(DFLASH_ERR_INVALID_ARG, "hidden is not 16-byte aligned");
+    if (c->shard_rows != c->cfg.V)
+        return fail(DFLASH_ERR_INVALID_ARG, "a vocabulary-shard handle runs through dflash_select_topk_shard and "
+                                            "dflash_select_run_gathered");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Plan pl = c->plan(B);
+    dflash_status st = launch_lmhead(c, hidden, pl, s);
+    if (st != DFLASH_OK) return st;
+    return launch_tail(c, anchor, B, pl, c->part, pl.G, u_walk, topk_ids, topk_vals, pair_scores, path, draft_probs,
+                       path_score, tie_flags, s);
+}
+
+dflash_status dflash_select_topk_shard(dflash_select_handle h, const void *hidden, int32_t B, uint64_t *shard_keys,
+                                       void *stream)
+{
+    if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+    dflash_select_ctx *c = h;
+    if (B < 0 || B > c->cfg.max_batch)
+        return fail(DFLASH_ERR_INVALID_ARG, "B must be in [0, max_batch=%d] (got %d)", c->cfg.max_batch, B);
+    if (B == 0) return ok();
+    if (!hidden || !shard_keys) return fail(DFLASH_ERR_INVALID_ARG, "hidden and shard_keys must not be NULL");
+    if (!aligned16(hidden)) return fail(DFLASH_ERR_INVALID_ARG, "hidden is not 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const Plan pl = c->plan(B);
+    const bool prof = c->prof;  // per-kernel timing covers whole runs only
+    c->prof = false;
+    dflash_status st = launch_lmhead(c, hidden, pl, s);
+    c->prof = prof;
+    if (st != DFLASH_OK) return st;
+    CUDA_TRY(dfl::launch_topk_merge(c->part, pl.G, pl.N, c->cfg.K, c->ids, c->vals, nullptr, nullptr, c->thr_g, s,
+                                    shard_keys));
+    return ok();
+}
+
+dflash_status dflash_select_run_gathered(dflash_select_handle h, const int32_t *anchor, int32_t B,
+                                         const uint64_t *all_keys, int32_t G, int32_t *topk_ids, float *topk_vals,
+                                         float *pair_scores, int32_t *path, float *path_score, uint8_t *tie_flags,
+                                         void *stream)
+{
+    if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
+    dflash_select_ctx *c = h;
+    if (c->cfg.walk == DFLASH_WALK_SAMPLE)
+        return fail(DFLASH_ERR_INVALID_ARG, "dflash_select_run_gathered takes the max-sum or the greedy walk");
+    if (B < 0 || B > c->cfg.max_batch)
+        return fail(DFLASH_ERR_INVALID_ARG, "B must be in [0, max_batch=%d] (got %d)", c->cfg.max_batch, B);
+    if (G < 1 || G > 1024) return fail(DFLASH_ERR_INVALID_ARG, "G must be in [1, 1024] (got %d)", G);
+    if (B == 0) return ok();
+    if (!anchor || !all_keys || !path) return fail(DFLASH_ERR_INVALID_ARG, "anchor, all_keys and path must not be NULL");
+    const Plan pl = c->plan(B);
+    const bool prof = c->prof;  // per-kernel timing covers whole runs only
+    c->prof = false;
+    const dflash_status st = launch_tail(c, anchor, B, pl, all_keys, G, nullptr, topk_ids, topk_vals, pair_scores,
+                                         path, nullptr, path_score, tie_flags, static_cast<cudaStream_t>(stream));
+    c->prof = prof;
+    return st;
 }
 
 dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,

@@ -74,7 +74,8 @@ struct LmHeadParams {
     CUtensorMap tm_w;     // lm_head W [V, d] bf16, box 64 x 128, 128B swizzle
     CUtensorMap tm_gate;  // W_H [256, d] bf16, box 64 x 128
     CUtensorMap tm_h;     // hidden [N, d] bf16, box 64 x NT
-    int64_t V;
+    int64_t V;            // rows of tm_w (a vocabulary shard's rows when id_base > 0)
+    uint32_t id_base = 0; // token id of row 0 of tm_w
     int d, N, NT, n_tiles_n, K;
     int m_tiles_vocab, m_tiles_total, ctas_per_ntile, stages;
     int boxes;        // 64-column TMA boxes per pipeline stage (d % (64 * boxes) == 0)
@@ -91,9 +92,12 @@ size_t lmhead_smem_bytes(int NT, int K, int stages, int boxes);
 int lmhead_boxes(int d, int NT);
 cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s);
 
-// Merges the partial lists of every CTA into the sorted top-K of each position.
+// Merges the partial lists of every CTA (or of every vocabulary shard: the
+// same [G][N][K] layout) into the sorted top-K of each position; keys_out
+// (optional) receives the merged keys [N][K].
 cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws,
-                              float *vals_ws, int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s);
+                              float *vals_ws, int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s,
+                              uint64_t *keys_out = nullptr);
 
 // ---- candidate projections A|B = [W_A; W_B] E[row] (tcgen05, projection.cu) ----
 struct ProjParams {

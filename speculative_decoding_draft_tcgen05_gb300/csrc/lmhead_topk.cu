@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                             const int col = c0 + jj;
                             const uint32_t slot = atomicAdd(col_cnt + col, 1u);
                             if (slot < static_cast<uint32_t>(capc))
-                                bucket[slot * NT + col] = make_key(pick16(v, jj), static_cast<uint32_t>(row0 + row));
+                                bucket[slot * NT + col] = make_key(pick16(v, jj), p.id_base + static_cast<uint32_t>(row0 + row));
                             else
                                 ovf[j & 1] = 1;
                         }
@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                             uint64_t x = 0ull;
                             if (b0 + lane < nsort) {
                                 const int r = scr[b0 + lane];
-                                x = make_key(T[cc * kLmTileM + r], static_cast<uint32_t>(row0 + r));
+                                x = make_key(T[cc * kLmTileM + r], p.id_base + static_cast<uint32_t>(row0 + r));
                             }
                             x = warp_sort_desc(x, lane);
                             mine = list_merge(mine, x, lane, K);
@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                             while (sv) {
                                 const int r = qq * 32 + __ffs(sv) - 1;
                                 sv &= sv - 1;
-                                const uint64_t x = make_key(T[cc * kLmTileM + r], static_cast<uint32_t>(row0 + r));
+                                const uint64_t x = make_key(T[cc * kLmTileM + r], p.id_base + static_cast<uint32_t>(row0 + r));
                                 if (x > th) {
                                     mine = list_insert(mine, x, lane, K);
                                     const uint64_t kth = shfl_u64(mine, K - 1);
@@ -720,7 +720,8 @@ constexpr int kMergeWarps = 16;
 __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint64_t *__restrict__ part, int G,
                                                                       int N, int K, int32_t *ids_ws,
                                                                       float *vals_ws, int32_t *ids_out,
-                                                                      float *vals_out, uint64_t *thr_g)
+                                                                      float *vals_out, uint64_t *thr_g,
+                                                                      uint64_t *keys_out)
 {
     extern __shared__ uint64_t mlists[];  // [G][K]
     __shared__ uint64_t wl[kMergeWarps][32];
@@ -768,6 +769,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint
         vals_ws[o] = v;
         if (ids_out) ids_out[o] = id;
         if (vals_out) vals_out[o] = v;
+        if (keys_out) keys_out[o] = run;
     }
 }
 
@@ -804,11 +806,11 @@ cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cud
 }
 
 cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws, float *vals_ws,
-                              int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s)
+                              int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s, uint64_t *keys_out)
 {
     const size_t smem = static_cast<size_t>(G) * K * sizeof(uint64_t);
     return launch_ex(topk_merge_kernel, dim3(N), dim3(kMergeWarps * 32), smem, s, 1, part, G, N, K, ids_ws,
-                     vals_ws, ids_out, vals_out, thr_g);
+                     vals_ws, ids_out, vals_out, thr_g, keys_out);
 }
 
 }  // namespace dfl
