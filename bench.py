@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tables", action="store_true",
                     help="precompute A|B for every token at init and gather table rows (a variant)")
+    ap.add_argument("--dedup", action="store_true",
+                    help="project each distinct token of a batch once on the larger-batch path (a variant)")
     ap.add_argument("--mode", default="max-sum", choices=["max-sum", "sample", "conv"],
                     help="max-sum walk + greedy accept check (default), sampling walk + rejection sampling, or the "
                          "drafter's two-tap dynamic convolution over the workload's blocks")
@@ -141,10 +143,11 @@ def committed_traffic(workload):
         return None
 
 
-def algorithmic_bytes(w, G, N, tables=False):
+def algorithmic_bytes(w, G, N, tables=False, distinct_rows=None):
     """Bytes the selector must move per step (see the design notes): the whole
     path and, separately, the lm_head+top-K kernel. With precomputed tables the
-    E-row gathers and the W_A/W_B reads become gathers of fp32 A|B table rows."""
+    E-row gathers and the W_A/W_B reads become gathers of fp32 A|B table rows;
+    with deduplication only ``distinct_rows`` E rows are gathered and projected."""
     d, V, L, K, B, e = w.d, w.V, w.L, w.K, w.B, w.e
     k1 = (V * d * 2            # lm_head weight, read once
           + e * d * 2          # W_H (the gate rows share the pass)
@@ -152,12 +155,13 @@ def algorithmic_bytes(w, G, N, tables=False):
           + G * N * K * 8      # partial top-K lists written
           + N * e * 4)         # gate g written
     R = L * K + 1
+    P = B * R if distinct_rows is None else distinct_rows  # rows projected
     rest = (G * N * K * 8      # partial lists read by the merge
             + N * K * 8        # merged ids + values
             + (B * R * 2 * e * 4 if tables else  # gathered table rows
-               B * R * d * 2      # gathered E rows
+               P * d * 2          # gathered E rows
                + 2 * e * d * 2    # W_A, W_B
-               + B * R * 2 * e * 4 * 2)  # projections written and read
+               + P * 2 * e * 4 + B * R * 2 * e * 4)  # projections written, read by the pair tables
             + N * e * 4        # gate read
             + N * K * K * 4    # pair tables written
             + B * (L + 1) * 4 + B * L * 4 * 2 + B * 4 + B * (L + 1) * 4)  # path, target, accept, emitted
@@ -226,17 +230,25 @@ def cpu_baseline(inp, seconds):
     b = wl.bf16_bits
     Wb, Eb, WAb, WBb, WHb = b(inp.W), b(inp.E), b(inp.W_A), b(inp.W_B), b(inp.W_H)
     cores = len(os.sched_getaffinity(0))
-    n, t0 = 0, time.perf_counter()
-    while True:
-        s = n % inp.wl.B
-        oracle.select(Wb, Eb, WAb, WBb, WHb, b(inp.hidden[s]), int(inp.anchor[s]), inp.wl.K, nthreads=cores)
-        n += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
+
+    def timed(threads, budget):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            s = n % inp.wl.B
+            oracle.select(Wb, Eb, WAb, WBb, WHb, b(inp.hidden[s]), int(inp.anchor[s]), inp.wl.K, nthreads=threads)
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= budget:
+                return n, el
+
+    n, el = timed(cores, seconds)
+    # the same oracle on one thread: at least one whole block, within about a third of the budget
+    n1, el1 = timed(1, seconds / 3)
     return {"value": n / el, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} whole blocks (one sequence each) of the {inp.wl.name} workload through the fp64 C "
-                      f"oracle with OpenMP over {cores} threads, {el:.1f} s"}
+                      f"oracle with OpenMP over {cores} threads, {el:.1f} s",
+            "single_thread": {"value": n1 / el1, "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} whole blocks on one thread, {el1:.1f} s"}}
 
 
 def run_reference(args):
@@ -356,7 +368,7 @@ def run_ours(args):
     sample = args.mode == "sample"
     sel = pkg.Selector(W, E, WA, WB, WH, L=w.L, K=w.K, max_batch=w.B,
                        walk=pkg.DFLASH_WALK_SAMPLE if sample else pkg.DFLASH_WALK_VITERBI, temperature=1.0,
-                       tables=args.tables)
+                       tables=args.tables, dedup=args.dedup)
     out = sel.outputs(w.B, full=False)
     accept = torch.empty(w.B, dtype=torch.int32, device=dev)
     emitted = torch.empty(w.B, w.L + 1, dtype=torch.int32, device=dev)
@@ -453,7 +465,12 @@ def run_ours(args):
     launches_per_step = pkg.dflash_select_launches_per_run(sel.h, w.B) + 1
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     N, NT, n_tiles, G = lmhead_geometry(w, sms)
-    k1_bytes, all_bytes = algorithmic_bytes(w, G, N, args.tables)
+    distinct = None
+    if args.dedup:  # the distinct gathered tokens of the workload's batch (x0 and every candidate)
+        full = sel.run(hidden, anchor)
+        torch.cuda.synchronize()
+        distinct = len(set(full["topk_ids"].flatten().tolist()) | set(anchor.tolist()))
+    k1_bytes, all_bytes = algorithmic_bytes(w, G, N, args.tables, distinct)
     k1_ms, k1_n = prof["lmhead_topk"]
     k1_avg_s = k1_ms / max(1, k1_n) / 1e3
     peak, peak_kind = hbm_peak()
@@ -472,7 +489,9 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.label, "B": w.B, "L": w.L, "K": w.K, "V": w.V, "d": w.d, "e": w.e,
-                       "variant": "precomputed A|B tables" if args.tables else "projections per run (the pages' form)",
+                       "variant": ("precomputed A|B tables" if args.tables else
+                                   "projections per run, each distinct token once" if args.dedup else
+                                   "projections per run (the pages' form)"),
                        "seed": w.seed, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (lm_head weight %.0f MB > 129 MB L2), no flush" % (w.V * w.d * 2 / 1e6)},
             "hbm_gbs_step": all_bytes / step_s / 1e9,

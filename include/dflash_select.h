@@ -77,6 +77,12 @@ typedef struct {
                            V x 512 fp32 (311 MB at V = 151,936; one GEMM over E of about a
                            millisecond), and gather table rows in every run. Same results up to fp32
                            summation order; a variant of this library, not of the pages. */
+    int32_t dedup;      /* 0: project every gathered row; 1: on the larger-batch path (the one that
+                           runs separate merge, projection and pair-table kernels), project each
+                           distinct token of the batch once (x0 and the candidates of every position
+                           and sequence) and let the pair tables read its row. Identical results; needs
+                           8 bytes per vocabulary token of workspace; not with tables = 1. A variant of
+                           this library, not of the pages. */
 } dflash_select_config;
 
 typedef struct dflash_select_ctx *dflash_select_handle;
@@ -175,12 +181,14 @@ dflash_status dflash_select_step_host(dflash_select_handle h, const void *hidden
 dflash_status dflash_select_sync_status(dflash_select_handle h, void *stream);
 
 /* Per-kernel timing of later runs with CUDA events on the run's stream
- * (enable = 1 turns it on and clears the record, 0 turns it off). */
+ * (enable = 1 turns it on and clears the record, 0 turns it off). Covers
+ * dflash_select_run and dflash_select_run_sampled. */
 dflash_status dflash_select_profile(dflash_select_handle h, int32_t enable);
 
 /* Reads the record: for kernel index k (0 = lm_head+top-K, 1 = merge,
  * 2 = projection, 3 = pair tables + walk, 4 = the fused small-batch tail that
- * replaces 1..3), total milliseconds and launch count over the recorded runs
+ * replaces 1..3, 5 = the deduplication of cfg.dedup), total milliseconds and
+ * launch count over the recorded runs
  * (at most 4096 runs are recorded). Waits for the recorded events.
  * n_kernels receives the number of kernel indices. */
 dflash_status dflash_select_profile_read(dflash_select_handle h, double *ms_total,

@@ -30,7 +30,7 @@ DFLASH_WALK_VITERBI = 0
 DFLASH_WALK_GREEDY = 1
 DFLASH_WALK_SAMPLE = 2
 
-KERNEL_NAMES = ("lmhead_topk", "topk_merge", "projection", "pair_walk", "select_tail")
+KERNEL_NAMES = ("lmhead_topk", "topk_merge", "projection", "pair_walk", "select_tail", "dedup")
 
 
 class DflashError(RuntimeError):
@@ -42,7 +42,8 @@ class DflashError(RuntimeError):
 class dflash_select_config(ctypes.Structure):
     _fields_ = [("V", ctypes.c_int64), ("d", ctypes.c_int32), ("L", ctypes.c_int32), ("K", ctypes.c_int32),
                 ("e", ctypes.c_int32), ("max_batch", ctypes.c_int32), ("walk", ctypes.c_int32),
-                ("tie_eps", ctypes.c_float), ("temperature", ctypes.c_float), ("tables", ctypes.c_int32)]
+                ("tie_eps", ctypes.c_float), ("temperature", ctypes.c_float), ("tables", ctypes.c_int32),
+                ("dedup", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -126,13 +127,16 @@ def _stream(stream):
 
 
 def dflash_select_init(W, E, W_A, W_B, W_H, *, L: int, K: int, max_batch: int, walk: int = DFLASH_WALK_VITERBI,
-                       tie_eps: float = 1e-3, temperature: float = 1.0, tables: bool = False, stream=None):
+                       tie_eps: float = 1e-3, temperature: float = 1.0, tables: bool = False, dedup: bool = False,
+                       stream=None):
     """Creates a selector handle over device bf16 weights W [V, d], E [V, d], W_A/W_B/W_H [256, d]
-    (tables=True: precompute A|B for every token at init and gather table rows in every run)."""
+    (tables=True: precompute A|B for every token at init and gather table rows in every run;
+    dedup=True: project each distinct token of a batch once on the larger-batch path)."""
     import torch
     V, d = W.shape
     cfg = dflash_select_config(V=V, d=d, L=L, K=K, e=W_A.shape[0], max_batch=max_batch, walk=walk,
-                               tie_eps=tie_eps, temperature=temperature, tables=1 if tables else 0)
+                               tie_eps=tie_eps, temperature=temperature, tables=1 if tables else 0,
+                               dedup=1 if dedup else 0)
     h = ctypes.c_void_p()
     _check(lib().dflash_select_init(ctypes.byref(cfg), _ptr(W, torch.bfloat16, "W"), _ptr(E, torch.bfloat16, "E"),
                                     _ptr(W_A, torch.bfloat16, "W_A"), _ptr(W_B, torch.bfloat16, "W_B"),
@@ -367,12 +371,12 @@ class Selector:
     """Owns a handle and the output tensors of one batch size (convenience only)."""
 
     def __init__(self, W, E, W_A, W_B, W_H, *, L, K, max_batch, walk=DFLASH_WALK_VITERBI, tie_eps=1e-3,
-                 temperature=1.0, tables=False):
+                 temperature=1.0, tables=False, dedup=False):
         import torch
         self.L, self.K, self.max_batch = L, K, max_batch
         self.device = W.device
         self.h = dflash_select_init(W, E, W_A, W_B, W_H, L=L, K=K, max_batch=max_batch, walk=walk, tie_eps=tie_eps,
-                                    temperature=temperature, tables=tables)
+                                    temperature=temperature, tables=tables, dedup=dedup)
         self._weights = (W, E, W_A, W_B, W_H)  # the handle borrows them: keep them alive with it
         self._torch = torch
 

@@ -106,11 +106,38 @@ dflash_status host_make_tmap(CUtensorMap *tm, const void *ptr, int64_t rows, int
 namespace {
 
 constexpr int kProfileRuns = 4096;
-constexpr int kProfileKernels = 5;  // lm_head+top-K, merge, projection, pair+walk, fused tail
-constexpr int kProfileSlots = 4;    // launches recorded per run
+constexpr int kProfileKernels = 6;  // lm_head+top-K, merge, projection, pair+walk, fused tail, dedup
+constexpr int kProfileSlots = 5;    // launches recorded per run
+
+// A pilot lm_head pass over kPilotTiles sampled vocabulary tiles (per
+// position tile) seeds the thresholds of position tiles at least
+// DFL_LM_PILOT_MIN_NT wide.
+constexpr int kPilotTiles = 64;
+#ifndef DFL_LM_PILOT_MIN_NT
+#define DFL_LM_PILOT_MIN_NT 96
+#endif
+#ifndef DFL_LM_PILOT_MAX_NTILES
+#define DFL_LM_PILOT_MAX_NTILES 16
+#endif
+
+// Position counts in (128, 256] run the CTA-pair lm_head kernel (one
+// 256-row weight tile per pair, half of the positions in each CTA's shared
+// memory): a single-CTA tile of that width holds less weight in flight per
+// SM than the HBM stream needs.
+#ifndef DFL_LM_PAIR
+#define DFL_LM_PAIR 1
+#endif
+#ifndef DFL_LM_PAIR_BOXES
+#define DFL_LM_PAIR_BOXES 1
+#endif
 
 struct Plan {
     int N, NT, n_tiles_n, G, grid, stages, boxes, R_total;
+    bool pair;                    // the CTA-pair kernel (one position tile, G = 2 x pairs)
+    int mt_vocab, mt_total;       // weight tiles of the pass (a pair: vocabulary tiles rounded up to even)
+    int pilot_G, pilot_stride;  // pilot CTAs per position tile and their tile stride (0: no pilot)
+    int pilot_stages, pilot_boxes;
+    size_t pilot_smem;
     size_t smem;
     bool fused_tail;  // one clustered kernel for merge + projections + tables + walk
     int tail_cs, tail_S;
@@ -131,15 +158,18 @@ struct dflash_select_ctx {
     size_t smem_optin = 0;  // opt-in shared memory per block
     CUtensorMap tm_w, tm_gate, tm_h, tm_wa, tm_wb;
     CUtensorMap tm_pa[3], tm_pb[3];  // W_A, W_B with 64 x {64, 128, 256}-row boxes (projection tiles)
-    const void *h_ptr = nullptr;
-    int h_rows = -1;
+    const void *h_ptr = nullptr, *hp_ptr = nullptr;
+    int h_rows = -1, h_box = -1, hp_rows = -1, hp_box = -1;
+    CUtensorMap tm_hp;  // hidden with whole-tile boxes, for the pilot of a pair pass
     int m_tiles_vocab = 0, m_tiles_total = 0, R = 0;
+    int pair_clusters = 0;  // CTA pairs of the pair lm_head kernel that fit at once (0: not used)
     int64_t shard_v0 = 0, shard_rows = 0;  // the rows of W_lm this handle streams: tokens [v0, v0 + rows)
 
     void *ws = nullptr;
     uint64_t *part = nullptr;
     uint64_t *thr_g = nullptr;  // per-position lm_head thresholds shared by the CTAs
     uint64_t *tmax = nullptr;   // [num_sms][max_batch * L] best logit of each lm_head CTA, epoch-tagged
+    uint64_t *pmax = nullptr;   // [kPilotTiles][max_batch * L] the pilot's tile maxima, epoch-tagged
     uint32_t epoch = 0;
     float *gate = nullptr, *vals = nullptr, *AB = nullptr, *P = nullptr;
     float *tab = nullptr;  // [V][512] precomputed A|B of every token (cfg.tables)
@@ -147,6 +177,10 @@ struct dflash_select_ctx {
     unsigned *ticket = nullptr;
     float *proj_part = nullptr;     // [2][rows][512] partial sums of the split projection
     unsigned *proj_ticket = nullptr;
+    uint64_t *dd_tab = nullptr;  // [V] deduplication marks (cfg.dedup)
+    unsigned *dd_count = nullptr;
+    int32_t *dd_uniq = nullptr, *dd_rep = nullptr;  // [max_batch * R]
+    uint32_t dd_epoch = 0;
     int *err = nullptr;
     // staging of dflash_select_step_host
     uint16_t *st_hidden = nullptr;
@@ -168,27 +202,64 @@ struct dflash_select_ctx {
 #ifndef DFL_LM_TILE_POS
 #define DFL_LM_TILE_POS 128
 #endif
-        if (p.N <= 256) {
+        p.pair = DFL_LM_PAIR && p.N > 128 && p.N <= 256 && pair_clusters > 0;
+        if (p.pair) {
+            p.n_tiles_n = 1;
+            p.NT = (p.N + 15) / 16 * 16;
+        } else if (p.N <= 256) {
             p.n_tiles_n = (p.N + DFL_LM_TILE_POS - 1) / DFL_LM_TILE_POS;
             p.NT = (((p.N + p.n_tiles_n - 1) / p.n_tiles_n) + 15) / 16 * 16;
         } else {
             p.NT = 256;
             p.n_tiles_n = (p.N + 255) / 256;
         }
-        int g = num_sms / p.n_tiles_n;
-        if (g < 1) g = 1;
-        if (g > m_tiles_total) g = m_tiles_total;
-        p.G = g;
-        p.grid = g * p.n_tiles_n;
-        p.boxes = dfl::lmhead_boxes(cfg.d, p.NT);
-        const size_t fixed = dfl::lmhead_smem_bytes(p.NT, cfg.K, 0, p.boxes);
-        const size_t stage = static_cast<size_t>(p.boxes) *
-                             (static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 +
-                              static_cast<size_t>(p.NT) * dfl::kLmTileK * 2);
-        int st = static_cast<int>((smem_optin - fixed) / stage);
-        if (st > dfl::kLmMaxStages) st = dfl::kLmMaxStages;
-        p.stages = st;
-        p.smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, st, p.boxes);
+        p.mt_vocab = p.pair ? (m_tiles_vocab + 1) / 2 * 2 : m_tiles_vocab;
+        p.mt_total = p.mt_vocab + dfl::kEmbed / dfl::kLmTileM;
+        // stages that fit for `boxes` boxes of weights and `hrows` hidden rows each
+        auto stages_for = [&](int NT, int boxes, int hrows) {
+            const size_t fixed = dfl::lmhead_smem_bytes(NT, cfg.K, 0, boxes, hrows);
+            const size_t stage = static_cast<size_t>(boxes) * (static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 +
+                                                               static_cast<size_t>(hrows) * dfl::kLmTileK * 2);
+            int st = static_cast<int>((smem_optin - fixed) / stage);
+            if (st > dfl::kLmMaxStages) st = dfl::kLmMaxStages;
+            while (st > 1 && dfl::lmhead_smem_bytes(NT, cfg.K, st, boxes, hrows) > smem_optin) --st;  // barriers
+            return st;
+        };
+        int hrows = p.NT;
+        if (p.pair) {
+            int g2 = num_sms / 2;
+            if (g2 > pair_clusters) g2 = pair_clusters;
+            if (g2 > p.mt_total / 2) g2 = p.mt_total / 2;
+            p.G = 2 * g2;
+            p.grid = 2 * g2;
+            p.boxes = DFL_LM_PAIR_BOXES;
+            while (p.boxes > 1 && cfg.d % (dfl::kLmTileK * p.boxes) != 0) --p.boxes;
+            hrows = p.NT / 2;
+        } else {
+            int g = num_sms / p.n_tiles_n;
+            if (g < 1) g = 1;
+            if (g > m_tiles_total) g = m_tiles_total;
+            p.G = g;
+            p.grid = g * p.n_tiles_n;
+            p.boxes = dfl::lmhead_boxes(cfg.d, p.NT);
+        }
+        p.stages = stages_for(p.NT, p.boxes, hrows);
+        p.smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, p.stages, p.boxes, hrows);
+        p.pilot_G = 0;
+        p.pilot_stride = 0;
+        p.pilot_boxes = p.boxes;
+        p.pilot_stages = p.stages;
+        p.pilot_smem = p.smem;
+        if (p.NT >= DFL_LM_PILOT_MIN_NT && p.n_tiles_n <= DFL_LM_PILOT_MAX_NTILES &&
+            m_tiles_vocab >= 4 * kPilotTiles) {
+            p.pilot_G = kPilotTiles;
+            p.pilot_stride = m_tiles_vocab / kPilotTiles;
+            if (p.pair) {  // the pilot runs the single-CTA kernel over the whole position tile
+                p.pilot_boxes = dfl::lmhead_boxes(cfg.d, p.NT);
+                p.pilot_stages = stages_for(p.NT, p.pilot_boxes, p.NT);
+                p.pilot_smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, p.pilot_stages, p.pilot_boxes);
+            }
+        }
         p.R_total = B * R;
         p.tail_cs = dfl::tail_cluster_size(cfg.d);
         p.tail_S = dfl::tail_stages(cfg.K, p.G, p.tail_cs, static_cast<int>(smem_optin));
@@ -262,6 +333,9 @@ static dflash_status check_config(const dflash_select_config *c)
     if (!(c->tie_eps >= 0.0f) || !std::isfinite(c->tie_eps))
         return fail(DFLASH_ERR_INVALID_ARG, "tie_eps must be finite and >= 0");
     if (c->tables != 0 && c->tables != 1) return fail(DFLASH_ERR_INVALID_ARG, "tables must be 0 or 1");
+    if (c->dedup != 0 && c->dedup != 1) return fail(DFLASH_ERR_INVALID_ARG, "dedup must be 0 or 1");
+    if (c->dedup && c->tables)
+        return fail(DFLASH_ERR_INVALID_ARG, "dedup applies to the per-run projections, not to tables = 1");
     return ok();
 }
 
@@ -305,6 +379,14 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     c->m_tiles_vocab = static_cast<int>((rows + dfl::kLmTileM - 1) / dfl::kLmTileM);
     c->m_tiles_total = c->m_tiles_vocab + dfl::kEmbed / dfl::kLmTileM;
     c->R = cfg->L * cfg->K + 1;
+    {
+        // CTA pairs resident at once, for the widest pair configuration (256
+        // positions; every configuration holds one CTA per SM)
+        const size_t fixed = dfl::lmhead_smem_bytes(256, cfg->K, 0, 1, 128);
+        const size_t stage = static_cast<size_t>(dfl::kLmTileM) * dfl::kLmTileK * 2 + 128u * dfl::kLmTileK * 2;
+        const size_t smem_pair = fixed + ((prop.sharedMemPerBlockOptin - fixed) / stage) * stage;
+        c->pair_clusters = dfl::lmhead_pair_max_clusters(smem_pair);
+    }
 
     if ((st = make_tmap(&c->tm_w, W_lm, rows, cfg->d, dfl::kLmTileM)) != DFLASH_OK ||
         (st = make_tmap(&c->tm_gate, W_H, dfl::kEmbed, cfg->d, dfl::kLmTileM)) != DFLASH_OK ||
@@ -334,6 +416,7 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     const size_t o_part = off; off += up(part_elems * 8);
     const size_t o_thrg = off; off += up(Nmax * 8);
     const size_t o_tmax = off; off += up(static_cast<size_t>(prop.multiProcessorCount) * Nmax * 8);
+    const size_t o_pmax = off; off += up(static_cast<size_t>(kPilotTiles) * Nmax * 8);
     const size_t o_gate = off; off += up(Nmax * dfl::kEmbed * 4);
     const size_t o_ids = off; off += up(Nmax * cfg->K * 4);
     const size_t o_vals = off; off += up(Nmax * cfg->K * 4);
@@ -345,6 +428,11 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
         std::min(static_cast<size_t>(dfl::projection_split_rows(prop.multiProcessorCount)), Bm * c->R);
     const size_t o_ppart = off; off += up(2 * split_rows * 512 * 4);
     const size_t o_ptick = off; off += up(static_cast<size_t>(8 * (prop.multiProcessorCount / 16 + 1)) * 4);
+    const size_t dd_rows = cfg->dedup ? Bm * c->R : 0;
+    const size_t o_ddtab = off; off += up(cfg->dedup ? static_cast<size_t>(cfg->V) * 8 : 0);
+    const size_t o_ddcnt = off; off += up(cfg->dedup ? 4 : 0);
+    const size_t o_dduniq = off; off += up(dd_rows * 4);
+    const size_t o_ddrep = off; off += up(dd_rows * 4);
     const size_t o_err = off; off += up(4);
     const size_t o_hid = off; off += up(Nmax * cfg->d * 2);
     const size_t o_anc = off; off += up(Bm * 4);
@@ -367,6 +455,7 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     c->part = reinterpret_cast<uint64_t *>(w + o_part);
     c->thr_g = reinterpret_cast<uint64_t *>(w + o_thrg);
     c->tmax = reinterpret_cast<uint64_t *>(w + o_tmax);
+    c->pmax = reinterpret_cast<uint64_t *>(w + o_pmax);
     c->gate = reinterpret_cast<float *>(w + o_gate);
     c->ids = reinterpret_cast<int32_t *>(w + o_ids);
     c->vals = reinterpret_cast<float *>(w + o_vals);
@@ -375,6 +464,12 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     c->ticket = reinterpret_cast<unsigned *>(w + o_ticket);
     c->proj_part = reinterpret_cast<float *>(w + o_ppart);
     c->proj_ticket = reinterpret_cast<unsigned *>(w + o_ptick);
+    if (cfg->dedup) {
+        c->dd_tab = reinterpret_cast<uint64_t *>(w + o_ddtab);
+        c->dd_count = reinterpret_cast<unsigned *>(w + o_ddcnt);
+        c->dd_uniq = reinterpret_cast<int32_t *>(w + o_dduniq);
+        c->dd_rep = reinterpret_cast<int32_t *>(w + o_ddrep);
+    }
     c->err = reinterpret_cast<int *>(w + o_err);
     c->st_hidden = reinterpret_cast<uint16_t *>(w + o_hid);
     c->st_anchor = reinterpret_cast<int32_t *>(w + o_anc);
@@ -459,11 +554,20 @@ static void prof_end(dflash_select_ctx *c, int slot, int kid, cudaStream_t s)
 // c->part, g_t in c->gate.
 static dflash_status launch_lmhead(dflash_select_ctx *c, const void *hidden, const Plan &pl, cudaStream_t s)
 {
-    if (hidden != c->h_ptr || pl.N != c->h_rows) {
-        dflash_status st = make_tmap(&c->tm_h, hidden, pl.N, c->cfg.d, pl.NT);
+    const int box = pl.pair ? pl.NT / 2 : pl.NT;
+    if (hidden != c->h_ptr || pl.N != c->h_rows || box != c->h_box) {
+        dflash_status st = make_tmap(&c->tm_h, hidden, pl.N, c->cfg.d, box);
         if (st != DFLASH_OK) return st;
         c->h_ptr = hidden;
         c->h_rows = pl.N;
+        c->h_box = box;
+    }
+    if (pl.pair && pl.pilot_G > 0 && (hidden != c->hp_ptr || pl.N != c->hp_rows || pl.NT != c->hp_box)) {
+        dflash_status st = make_tmap(&c->tm_hp, hidden, pl.N, c->cfg.d, pl.NT);
+        if (st != DFLASH_OK) return st;
+        c->hp_ptr = hidden;
+        c->hp_rows = pl.N;
+        c->hp_box = pl.NT;
     }
     dfl::LmHeadParams lp;
     lp.tm_w = c->tm_w;
@@ -476,8 +580,8 @@ static dflash_status launch_lmhead(dflash_select_ctx *c, const void *hidden, con
     lp.NT = pl.NT;
     lp.n_tiles_n = pl.n_tiles_n;
     lp.K = c->cfg.K;
-    lp.m_tiles_vocab = c->m_tiles_vocab;
-    lp.m_tiles_total = c->m_tiles_total;
+    lp.m_tiles_vocab = pl.mt_vocab;
+    lp.m_tiles_total = pl.mt_total;
     lp.ctas_per_ntile = pl.G;
     lp.stages = pl.stages;
     lp.boxes = pl.boxes;
@@ -490,7 +594,26 @@ static dflash_status launch_lmhead(dflash_select_ctx *c, const void *hidden, con
     lp.err = c->err;
 
     prof_begin(c, 0, s);
-    CUDA_TRY(dfl::launch_lmhead_topk(lp, pl.grid, pl.smem, s));
+    if (pl.pilot_G > 0) {
+        dfl::LmHeadParams pp = lp;
+        pp.pilot_stride = pl.pilot_stride;
+        pp.ctas_per_ntile = pl.pilot_G;
+        pp.m_tiles_vocab = c->m_tiles_vocab;
+        pp.m_tiles_total = c->m_tiles_total;
+        pp.stages = pl.pilot_stages;
+        pp.boxes = pl.pilot_boxes;
+        if (pl.pair) pp.tm_h = c->tm_hp;
+        pp.tmax = nullptr;
+        pp.pmax = c->pmax;
+        CUDA_TRY(dfl::launch_lmhead_topk(pp, pl.pilot_G * pl.n_tiles_n, pl.pilot_smem, s));
+        lp.tmax = nullptr;  // the pilot's maxima replace the CTAs' own
+        lp.pmax = c->pmax;
+        lp.pmax_n = pl.pilot_G;
+    }
+    if (pl.pair)
+        CUDA_TRY(dfl::launch_lmhead_topk_pair(lp, pl.grid, pl.smem, s));
+    else
+        CUDA_TRY(dfl::launch_lmhead_topk(lp, pl.grid, pl.smem, s));
     prof_end(c, 0, 0, s);
     return ok();
 }
@@ -550,9 +673,31 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
         return ok();
     }
 
-    prof_begin(c, 1, s);
-    CUDA_TRY(dfl::launch_topk_merge(part, G, pl.N, c->cfg.K, c->ids, c->vals, topk_ids, topk_vals, c->thr_g, s));
-    prof_end(c, 1, 1, s);
+    dfl::DedupParams dd;
+    if (c->dd_tab && !c->tab) {
+        dd.tab = c->dd_tab;
+        dd.count = c->dd_count;
+        dd.uniq = c->dd_uniq;
+        dd.rep = c->dd_rep;
+        dd.anchor = anchor;
+        dd.err = c->err;
+        dd.V = c->cfg.V;
+        dd.L = c->cfg.L;
+        dd.K = c->cfg.K;
+        dd.R = c->R;
+        dd.epoch = ++c->dd_epoch;
+        if (dd.epoch == 0) dd.epoch = ++c->dd_epoch;  // 0 is the zeroed table's mark
+    }
+    int slot = 1;  // profiling slots are filled in launch order
+    prof_begin(c, slot, s);
+    CUDA_TRY(dfl::launch_topk_merge(part, G, pl.N, c->cfg.K, c->ids, c->vals, topk_ids, topk_vals, c->thr_g, s,
+                                    nullptr, dd));
+    prof_end(c, slot++, 1, s);
+    if (dd.tab) {
+        prof_begin(c, slot, s);
+        CUDA_TRY(dfl::launch_dedup_compact(dd, c->ids, pl.R_total, s));
+        prof_end(c, slot++, 5, s);
+    }
 
     dfl::ProjParams pp;
     const int nc = dfl::projection_cols(pl.R_total, c->num_sms);
@@ -573,10 +718,14 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
     pp.ksplit = dfl::projection_ksplit(pl.R_total, nc, c->cfg.d, c->num_sms);
     pp.part = c->proj_part;
     pp.ticket = c->proj_ticket;
+    if (dd.tab) {
+        pp.uniq = c->dd_uniq;
+        pp.count = c->dd_count;
+    }
     if (!c->tab) {
-        prof_begin(c, 2, s);
+        prof_begin(c, slot, s);
         CUDA_TRY(dfl::launch_projection(pp, nc, s));
-        prof_end(c, 2, 2, s);
+        prof_end(c, slot++, 2, s);
     }
 
     dfl::PairParams q;
@@ -603,7 +752,10 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
     q.u_walk = u_walk;
     q.q_out = draft_probs;
     q.temperature = c->cfg.temperature;
-    const int slot = c->tab ? 2 : 3;  // profiling slots are filled in launch order
+    if (dd.tab) {
+        q.dd_tab = c->dd_tab;
+        q.dd_rep = c->dd_rep;
+    }
     prof_begin(c, slot, s);
     CUDA_TRY(dfl::launch_pair_walk(q, s));
     prof_end(c, slot, 3, s);
@@ -817,7 +969,8 @@ dflash_status dflash_select_profile_read(dflash_select_handle h, double *ms_tota
 int32_t dflash_select_launches_per_run(dflash_select_handle h, int32_t B)
 {
     if (!h || B <= 0 || B > h->cfg.max_batch) return 0;
-    return h->plan(B).fused_tail ? 2 : (h->tab ? 3 : 4);
+    const Plan pl = h->plan(B);
+    return (pl.pilot_G > 0 ? 1 : 0) + (pl.fused_tail ? 2 : (h->tab ? 3 : (h->dd_tab ? 5 : 4)));
 }
 
 dflash_status dflash_select_destroy(dflash_select_handle h)

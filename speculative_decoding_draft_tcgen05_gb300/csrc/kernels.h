@@ -86,18 +86,54 @@ struct LmHeadParams {
                       // `epoch` in the high word (NULL: not used)
     uint32_t epoch;   // differs between consecutive runs on the same tmax
     int *err;
+    // Sampled threshold ("pilot"). A pilot launch (pilot_stride > 0) gives each
+    // CTA the single vocabulary tile chunk * pilot_stride and publishes only its
+    // best logit per position to pmax[chunk][N] (epoch-tagged), nothing else.
+    // A main launch with pmax_n > 0 starts every position's threshold at the
+    // K-th largest of those pmax_n maxima (K tiles hold a logit at least that
+    // large) and takes the per-tile epilogue from its first tile.
+    int pilot_stride = 0;
+    uint64_t *pmax = nullptr;
+    int pmax_n = 0;
 };
 
-size_t lmhead_smem_bytes(int NT, int K, int stages, int boxes);
+// hrows: hidden rows per stage (NT; NT / 2 for the CTA-pair kernel)
+size_t lmhead_smem_bytes(int NT, int K, int stages, int boxes, int hrows = -1);
 int lmhead_boxes(int d, int NT);
 cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s);
+// The CTA-pair kernel: one position tile of NT <= 256 positions (tm_h boxes of
+// NT / 2 rows), 256-row weight tiles (m_tiles_vocab even: an odd vocabulary
+// tile count gets one tile past V, which reads as zeros), grid = 2 x pairs.
+cudaError_t launch_lmhead_topk_pair(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s);
+// Pairs of the CTA-pair kernel that fit on the device at once (0 if unknown).
+int lmhead_pair_max_clusters(size_t smem);
+
+// ---- candidate deduplication (a variant: each distinct token of a batch is projected once) ----
+// Gathered row gr of sequence b = gr / R is the anchor x0 (gr % R == 0) or
+// candidate gr % R - 1 of the sequence's [L][K] list. The merge marks, per
+// token, the first row that holds it: tab[token] = (epoch << 32) | ~row under
+// atomicMax, so a newer run's mark always wins and the table needs no reset.
+struct DedupParams {
+    uint64_t *tab = nullptr;  // [V] marks (NULL: no deduplication)
+    unsigned *count = nullptr;  // distinct tokens of the run (reset by the merge)
+    int32_t *uniq = nullptr;  // [B * R] the distinct tokens, in the order they were counted
+    int32_t *rep = nullptr;   // [B * R] at a token's first row: its index in uniq
+    const int32_t *anchor = nullptr;  // [B]
+    int *err = nullptr;
+    int64_t V = 0;
+    int L = 0, K = 0, R = 0;
+    uint32_t epoch = 0;
+};
+// uniq / rep from the marks, one thread per gathered row (R_total rows).
+cudaError_t launch_dedup_compact(const DedupParams &d, const int32_t *ids, int R_total, cudaStream_t s);
 
 // Merges the partial lists of every CTA (or of every vocabulary shard: the
 // same [G][N][K] layout) into the sorted top-K of each position; keys_out
-// (optional) receives the merged keys [N][K].
+// (optional) receives the merged keys [N][K]; with dd.tab the merged
+// candidates (and the anchors) are marked for deduplication.
 cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws,
                               float *vals_ws, int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s,
-                              uint64_t *keys_out = nullptr);
+                              uint64_t *keys_out = nullptr, const DedupParams &dd = DedupParams());
 
 // ---- candidate projections A|B = [W_A; W_B] E[row] (tcgen05, projection.cu) ----
 struct ProjParams {
@@ -112,6 +148,8 @@ struct ProjParams {
     int ksplit;                   // CTAs per output tile along d (1 or 2)
     float *part;                  // [ksplit][R_total][512] partial sums (ksplit > 1)
     unsigned *ticket;             // [row tiles][512 / NC] zero on entry, left zero (ksplit > 1)
+    const int32_t *uniq = nullptr;   // deduplicated rows: row gr < *count is token uniq[gr] (NULL: no
+    const unsigned *count = nullptr; // deduplication; R_total then only sizes the grid)
 };
 cudaError_t prepare_projection(int smem_optin);
 // Output columns per CTA (64, 128 or 256) for R_total gathered rows: the
@@ -145,6 +183,8 @@ struct PairParams {
     const float *u_walk;  // [B, L] uniforms (sampling walk)
     float *q_out;         // [B, L, K] draft distributions (sampling walk)
     float temperature;
+    const uint64_t *dd_tab = nullptr;  // deduplicated AB rows: the row of token v is
+    const int32_t *dd_rep = nullptr;   // dd_rep[~low32(dd_tab[v])] (NULL: AB by gathered row)
 };
 cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s);
 

@@ -41,6 +41,12 @@ constexpr int kBucketKeys = static_cast<int>(kTransposeBytes / 8);
 #ifndef DFL_LM_FAST_FROM
 #define DFL_LM_FAST_FROM 2
 #endif
+// Widest position tile that takes the per-tile path (measured at the 256-wide
+// tiles of 3840 positions: lm_head 2834 -> 2568 us at K = 16, 3417 -> 3074 us
+// at K = 32, against the chunked path throughout).
+#ifndef DFL_LM_FAST_MAXNT
+#define DFL_LM_FAST_MAXNT 256
+#endif
 
 // Inserts the keys bk[s * bstride] (s < n) that exceed th into the sorted list
 // l[i * LS] (i < KK, descending) of one position, in registers; th rises to
@@ -162,10 +168,12 @@ struct Layout {
         total;
 };
 
-__host__ __device__ inline Layout make_layout(int NT, int K, int stages, int boxes)
+// hrows: hidden rows a stage holds (NT, or NT / 2 in a CTA pair, which splits
+// the positions of a tile between its two CTAs)
+__host__ __device__ inline Layout make_layout(int NT, int K, int stages, int boxes, int hrows)
 {
     Layout l;
-    l.stage_bytes = static_cast<uint32_t>(boxes) * (kTileABytes + static_cast<uint32_t>(NT) * kLmTileK * 2);
+    l.stage_bytes = static_cast<uint32_t>(boxes) * (kTileABytes + static_cast<uint32_t>(hrows) * kLmTileK * 2);
     l.off_T = stages * l.stage_bytes;
     l.off_wscr = l.off_T + kTransposeBytes;
     l.off_list = l.off_wscr + 8 * kLmTileM;  // eight epilogue warps x 128 row indices
@@ -183,6 +191,11 @@ __host__ __device__ inline Layout make_layout(int NT, int K, int stages, int box
     return l;
 }
 
+// kPair: a cluster of two CTAs computes one 256-row tile (cta_group::2 MMAs
+// issued by the even CTA): each CTA holds 128 weight rows and half of the
+// tile's positions in its shared memory, and receives its 128 rows x NT
+// accumulator in its own tensor memory.
+template <bool kPair>
 __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid_constant__ LmHeadParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -192,8 +205,10 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
 
     const int NT = p.NT, K = p.K, S = p.stages;
     const int BX = p.boxes;  // 64-column boxes per stage
-    const Layout lay = make_layout(NT, K, S, BX);
+    const int HR = kPair ? NT / 2 : NT;  // hidden rows of a stage in this CTA
+    const Layout lay = make_layout(NT, K, S, BX, HR);
     const uint32_t w_bytes = static_cast<uint32_t>(BX) * kTileABytes;  // weight part of a stage
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;               // 0: issues the pair's MMAs
     float *const T = reinterpret_cast<float *>(gbase + lay.off_T);
     uint8_t *const wscr = gbase + lay.off_wscr;
     uint64_t *const lists = reinterpret_cast<uint64_t *>(gbase + lay.off_list);
@@ -224,6 +239,17 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     const int n_tile = blockIdx.x % p.n_tiles_n;
     const int chunk = blockIdx.x / p.n_tiles_n;
     const int G = p.ctas_per_ntile;
+    const bool pilot = !kPair && p.pilot_stride > 0;
+    // this CTA's tiles: chunk, chunk + G, ... (a pilot CTA: chunk * pilot_stride
+    // only; a pair: the two halves 2 q + rank of the pair's 256-row tiles q)
+    const int m_first = kPair ? chunk / 2 : (pilot ? chunk * p.pilot_stride : chunk);
+    const int m_step = kPair ? G / 2 : (pilot ? p.m_tiles_total : G);
+    const int n_my_tiles = kPair ? (p.m_tiles_total / 2 - m_first + m_step - 1) / m_step
+                                 : (pilot ? 1 : (p.m_tiles_total - chunk + G - 1) / G);
+    // the 128-row weight tile of this CTA's i-th tile (a pair's m_tiles_total is even)
+    auto tile_at = [&](int i) {
+        return kPair ? 2 * (m_first + i * m_step) + static_cast<int>(rank) : m_first + i * m_step;
+    };
     const int KB = p.d / (kLmTileK * BX);
     const uint32_t tmem_cols = tmem_cols_for(NT);
     const int C = acc_chains(NT);
@@ -236,7 +262,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         }
         for (int a = 0; a < 4; ++a) {
             mbar_init(bar_tfull + 8u * a, 1);
-            mbar_init(bar_tempty + 8u * a, 128);
+            mbar_init(bar_tempty + 8u * a, kPair ? 256 : 128);  // a pair: both CTAs' TMEM readers
         }
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
@@ -257,11 +283,17 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     }
     if (warp == 1) {
         __syncwarp();
-        tmem_alloc(smem_u32(tmem_holder), tmem_cols);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(smem_u32(tmem_holder), tmem_cols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), tmem_cols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();  // the even CTA's barriers are initialised before any use
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
     // The set-up above overlaps the previous kernel on the stream. Hidden
@@ -276,32 +308,41 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
 #ifdef DFL_LM_NOHINT
             const uint64_t pol_w = l2_policy_evict_normal();
 #else
-            const uint64_t pol_w = l2_policy_evict_first();  // weights: streamed once
+            // weights: streamed once; a pilot's rows are read again by the main pass
+            const uint64_t pol_w = pilot ? l2_policy_evict_last() : l2_policy_evict_first();
 #endif
             const uint64_t pol_h = l2_policy_evict_last();   // hidden: re-read by every CTA
-            const int n_my_tiles = (p.m_tiles_total - chunk + G - 1) / G;
             const int total = n_my_tiles * KB;
             // the first ring's weight tiles go out before the wait (the ring
             // starts empty, so no slot has to be waited for)
             const int pre = total < S ? total : S;
+            // a pair counts both CTAs' bytes on the even CTA's barriers
+            const uint32_t tx_bytes = kPair ? 2u * lay.stage_bytes : lay.stage_bytes;
+            const int hrow0 = n_tile * NT + static_cast<int>(rank) * HR;
+            auto load = [&](uint32_t dst, const CUtensorMap *tm, int x, int y, uint32_t bar, uint64_t pol) {
+                if constexpr (kPair)
+                    tma_load_2d_pair(dst, tm, x, y, mapa_shared(bar, 0), pol);
+                else
+                    tma_load_2d(dst, tm, x, y, bar, pol);
+            };
             for (int it = 0; it < pre; ++it) {
-                const int m = chunk + (it / KB) * G, kb = it % KB;
+                const int m = tile_at(it / KB), kb = it % KB;
                 const bool gate = m >= p.m_tiles_vocab;
                 const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
-                mbar_arrive_expect_tx(bar_full + 8u * it, lay.stage_bytes);
+                if (rank == 0) mbar_arrive_expect_tx(bar_full + 8u * it, tx_bytes);
                 for (int bx = 0; bx < BX; ++bx)
-                    tma_load_2d(base + it * lay.stage_bytes + bx * kTileABytes, gate ? &p.tm_gate : &p.tm_w,
-                                (kb * BX + bx) * kLmTileK, row0, bar_full + 8u * it, pol_w);
+                    load(base + it * lay.stage_bytes + bx * kTileABytes, gate ? &p.tm_gate : &p.tm_w,
+                         (kb * BX + bx) * kLmTileK, row0, bar_full + 8u * it, pol_w);
             }
             pdl_wait();
             for (int it = 0; it < pre; ++it)
                 for (int bx = 0; bx < BX; ++bx)
-                    tma_load_2d(base + it * lay.stage_bytes + w_bytes + bx * NT * kLmTileK * 2, &p.tm_h,
-                                ((it % KB) * BX + bx) * kLmTileK, n_tile * NT, bar_full + 8u * it, pol_h);
+                    load(base + it * lay.stage_bytes + w_bytes + bx * HR * kLmTileK * 2, &p.tm_h,
+                         ((it % KB) * BX + bx) * kLmTileK, hrow0, bar_full + 8u * it, pol_h);
             int it = pre;
             bool ok = true;
             for (; ok && it < total; ++it) {
-                const int m = chunk + (it / KB) * G, kb = it % KB;
+                const int m = tile_at(it / KB), kb = it % KB;
                 const bool gate = m >= p.m_tiles_vocab;
                 const CUtensorMap *tma = gate ? &p.tm_gate : &p.tm_w;
                 const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
@@ -312,30 +353,41 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     break;
                 }
                 const uint32_t sa = base + s * lay.stage_bytes;
-                mbar_arrive_expect_tx(bar_full + 8u * s, lay.stage_bytes);
+                if (rank == 0) mbar_arrive_expect_tx(bar_full + 8u * s, tx_bytes);
                 for (int bx = 0; bx < BX; ++bx)
-                    tma_load_2d(sa + bx * kTileABytes, tma, (kb * BX + bx) * kLmTileK, row0, bar_full + 8u * s, pol_w);
+                    load(sa + bx * kTileABytes, tma, (kb * BX + bx) * kLmTileK, row0, bar_full + 8u * s, pol_w);
                 for (int bx = 0; bx < BX; ++bx)
-                    tma_load_2d(sa + w_bytes + bx * NT * kLmTileK * 2, &p.tm_h, (kb * BX + bx) * kLmTileK,
-                                n_tile * NT, bar_full + 8u * s, pol_h);
+                    load(sa + w_bytes + bx * HR * kLmTileK * 2, &p.tm_h, (kb * BX + bx) * kLmTileK, hrow0,
+                         bar_full + 8u * s, pol_h);
             }
             if (!ok) {
                 atomicOr(p.err, DEV_ERR_TIMEOUT);
                 // let the copies already issued land before the CTA can exit
-                for (int j = (it > S ? it - S : 0); j < it; ++j)
-                    mbar_wait(bar_full + 8u * (j % S), static_cast<uint32_t>(j / S) & 1u, abort_flag, false);
+                if (rank == 0) {
+                    for (int j = (it > S ? it - S : 0); j < it; ++j)
+                        mbar_wait(bar_full + 8u * (j % S), static_cast<uint32_t>(j / S) & 1u, abort_flag, false);
+                } else {
+                    // the odd CTA of a pair cannot observe its copies (they are
+                    // counted on the even CTA's barriers): a copy lands within
+                    // microseconds, so it waits 100 us
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 100000ull) {
+                    }
+                }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kLmTileM, NT);
+        // ------------------------------------------------ MMA issuer (a pair: the even CTA's)
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kLmTileM : kLmTileM, NT);
             int it = 0, j = 0;
             bool ok = true;
-            for (int m = chunk; ok && m < p.m_tiles_total; m += G, ++j) {
+            for (; ok && j < n_my_tiles; ++j) {
                 const int a = j % NA;
                 const uint32_t u = static_cast<uint32_t>(j / NA);
-                if (!mbar_wait(bar_tempty + 8u * a, (u & 1u) ^ 1u, abort_flag)) {
+                const bool got = kPair ? mbar_wait_cluster(bar_tempty + 8u * a, (u & 1u) ^ 1u, abort_flag)
+                                       : mbar_wait(bar_tempty + 8u * a, (u & 1u) ^ 1u, abort_flag);
+                if (!got) {
                     ok = false;
                     break;
                 }
@@ -344,7 +396,9 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                 for (int kb = 0; kb < KB; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = static_cast<uint32_t>(it / S) & 1u;
-                    if (!mbar_wait(bar_full + 8u * s, ph, abort_flag)) {
+                    const bool full = kPair ? mbar_wait_cluster(bar_full + 8u * s, ph, abort_flag)
+                                            : mbar_wait(bar_full + 8u * s, ph, abort_flag);
+                    if (!full) {
                         ok = false;
                         break;
                     }
@@ -355,19 +409,34 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
 #pragma unroll
                         for (int k = 0; k < kLmTileK / 16; ++k) {
                             const int ks = bx * (kLmTileK / 16) + k;  // k-step within the stage
-                            umma_bf16(d_tmem + static_cast<uint32_t>((ks % C) * NT),
-                                      smem_desc_sw128(sa + bx * kTileABytes + 32u * k),
-                                      smem_desc_sw128(sb + bx * NT * kLmTileK * 2 + 32u * k), idesc,
-                                      (kb > 0 || ks >= C) ? 1u : 0u);
+                            const uint64_t ad = smem_desc_sw128(sa + bx * kTileABytes + 32u * k);
+                            const uint64_t bd = smem_desc_sw128(sb + bx * HR * kLmTileK * 2 + 32u * k);
+                            const uint32_t acc = (kb > 0 || ks >= C) ? 1u : 0u;
+                            if constexpr (kPair)
+                                umma_bf16_pair(d_tmem + static_cast<uint32_t>((ks % C) * NT), ad, bd, idesc, acc);
+                            else
+                                umma_bf16(d_tmem + static_cast<uint32_t>((ks % C) * NT), ad, bd, idesc, acc);
                         }
                     }
-                    umma_commit(bar_empty + 8u * s);  // frees the stage once these MMAs have read it
+                    // frees the stage (both CTAs' halves) once these MMAs have read it
+                    if constexpr (kPair)
+                        umma_commit_pair(bar_empty + 8u * s, 3);
+                    else
+                        umma_commit(bar_empty + 8u * s);
                 }
-                if (ok) umma_commit(bar_tfull + 8u * a);
+                if (ok) {
+                    if constexpr (kPair)
+                        umma_commit_pair(bar_tfull + 8u * a, 3);
+                    else
+                        umma_commit(bar_tfull + 8u * a);
+                }
             }
             if (!ok) atomicOr(p.err, DEV_ERR_TIMEOUT);
             // every MMA must be finished before TMEM is released
-            umma_commit(bar_drain);
+            if constexpr (kPair)
+                umma_commit_pair(bar_drain, 1);
+            else
+                umma_commit(bar_drain);
             mbar_wait(bar_drain, 0, abort_flag, false);
         }
     } else {
@@ -387,7 +456,16 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         int j = 0;
         int nchunk = 0;  // top-K chunks processed so far (selects the flag word)
         bool ok = true;
-        for (int m = chunk; m < p.m_tiles_total; m += G, ++j) {
+        const int fast_from = p.pmax_n > 0 ? 0 : DFL_LM_FAST_FROM;
+        // hands accumulator a back to the MMA warp (a pair: to the even CTA's)
+        auto release_acc = [&](int a) {
+            if constexpr (kPair)
+                mbar_arrive_remote(mapa_shared(bar_tempty + 8u * a, 0));
+            else
+                mbar_arrive(bar_tempty + 8u * a);
+        };
+        for (; j < n_my_tiles; ++j) {
+            const int m = tile_at(j);
             const int a = j % NA;
             const uint32_t u = static_cast<uint32_t>(j / NA);
             const bool gate = m >= p.m_tiles_vocab;
@@ -405,7 +483,11 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
             // Used where the list upkeep is the bottleneck (many positions per
             // CTA, measured: from about 100) and the n-tile has enough CTAs to
             // give K maxima.
-            const bool refresh = p.tmax && !gate && j == 2 && G >= 2 * K && nvalid >= 96;
+            // The pilot's maxima take the same path at the first tile.
+            const bool from_pilot = p.pmax_n > 0 && !gate && j == 0;
+            const bool refresh = from_pilot || (p.tmax && !gate && j == 2 && G >= 2 * K && nvalid >= 96);
+            const uint64_t *const rsrc = from_pilot ? p.pmax : p.tmax;
+            const int nsrc = from_pilot ? p.pmax_n : G;
             if (refresh) {
                 // Every CTA of this n-tile published its best logit per position
                 // after its first tile. If at least K of them are >= v, then K
@@ -417,7 +499,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
 #pragma unroll
                     for (int u2 = 0; u2 < 5; ++u2) {
                         const int g2 = lane + 32 * u2;
-                        t[u2] = g2 < G ? __ldcg(p.tmax + static_cast<size_t>(g2) * p.N + col_base + col) : 0ull;
+                        t[u2] = g2 < nsrc ? __ldcg(rsrc + static_cast<size_t>(g2) * p.N + col_base + col) : 0ull;
                     }
                     uint32_t best = 0;
 #pragma unroll
@@ -430,7 +512,9 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     if (lane == 0) rb[col] = kth << 32;  // any key of that logit value or above passes
                 }
             }
-            const bool got = tmem_warp ? mbar_wait(bar_tfull + 8u * a, u & 1u, abort_flag) : true;
+            const bool got = !tmem_warp ? true
+                             : kPair    ? mbar_wait_cluster(bar_tfull + 8u * a, u & 1u, abort_flag)
+                                        : mbar_wait(bar_tfull + 8u * a, u & 1u, abort_flag);
             if (refresh) named_bar_sync(1, 256);
             if (!gate) {
 #pragma unroll
@@ -455,7 +539,43 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
             const int row0 = (gate ? m - p.m_tiles_vocab : m) * kLmTileM;
             bool released = false;  // the accumulator is handed back to the MMA warp
             const int capc = kBucketKeys / NT;  // keys per position and tile
-            if (!gate && j >= DFL_LM_FAST_FROM && NT >= 32 && NT <= 128) {
+            if (pilot) {
+                // The pilot: per position, the best logit of this tile (rows past
+                // V count as nothing), one warp reduction per column and quadrant.
+                uint32_t *const qmax = reinterpret_cast<uint32_t *>(T);  // [4][NT]
+                if (tmem_warp) {
+                    const bool rowok = static_cast<int64_t>(row0) + row < p.V;
+                    for (int c0 = 0; c0 < ncols16; c0 += 16) {
+                        float v[16];
+                        __syncwarp();
+                        tmem_load16(taddr + static_cast<uint32_t>(c0), v);
+                        for (int c = 1; c < C; ++c) {
+                            float w[16];
+                            tmem_load16(taddr + static_cast<uint32_t>(c * NT + c0), w);
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) v[jj] += w[jj];
+                        }
+                        uint32_t mine = 0;
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const uint32_t o = __reduce_max_sync(0xFFFFFFFFu, rowok ? f32_to_ordered(v[jj]) : 0u);
+                            if (lane == jj) mine = o;
+                        }
+                        if (lane < 16 && c0 + lane < nvalid) qmax[q * NT + c0 + lane] = mine;
+                    }
+                    tc_fence_before_sync();
+                    release_acc(a);
+                }
+                named_bar_sync(1, 256);
+                for (int c = et; c < nvalid; c += 256) {
+                    uint32_t best = qmax[c];
+#pragma unroll
+                    for (int qq = 1; qq < 4; ++qq) best = max(best, qmax[qq * NT + c]);
+                    p.pmax[static_cast<size_t>(chunk) * p.N + col_base + c] = (static_cast<uint64_t>(p.epoch) << 32) | best;
+                }
+                continue;
+            }
+            if (!gate && j >= fast_from && NT >= 32 && NT <= DFL_LM_FAST_MAXNT) {
                 // Once the lists are warm few logits pass. All eight warps read
                 // the tile (warps w and w + 4 share a lane quadrant, each takes
                 // every other 16-column chunk), file the survivors by position,
@@ -511,7 +631,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                 }
                 if (ovf[j & 1] == 0) {  // uniform: all read the same flag
                     released = true;
-                    if (tmem_warp) mbar_arrive(bar_tempty + 8u * a);
+                    if (tmem_warp) release_acc(a);
                     if (nsurv > 0) {  // thread et owns position et
                         const int c = et;
                         uint64_t th = thr[c], kth = 0;
@@ -682,7 +802,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
             }
             if (tmem_warp && !released) {
                 tc_fence_before_sync();
-                mbar_arrive(bar_tempty + 8u * a);
+                release_acc(a);
             }
             if (p.tmax && !gate && j == 0) {
                 named_bar_sync(1, 256);  // the first tile's lists are complete
@@ -697,17 +817,21 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
         }
         if (!ok) atomicOr(p.err, DEV_ERR_TIMEOUT);
         named_bar_sync(1, 256);
-        for (int i = et; i < nvalid * K; i += 256) {
+        for (int i = et; !pilot && i < nvalid * K; i += 256) {
             const int col = i / K;
             p.part[(static_cast<size_t>(chunk) * p.N + col_base + col) * K + (i % K)] = lists[(i % K) * LS + col];
         }
     }
 
     __syncthreads();
+    if constexpr (kPair) cluster_sync_all();  // the pair's MMAs, copies and arrivals are over in both CTAs
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, tmem_cols);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem_base, tmem_cols);
+        else
+            tmem_dealloc(tmem_base, tmem_cols);
     }
 }
 
@@ -721,7 +845,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint
                                                                       int N, int K, int32_t *ids_ws,
                                                                       float *vals_ws, int32_t *ids_out,
                                                                       float *vals_out, uint64_t *thr_g,
-                                                                      uint64_t *keys_out)
+                                                                      uint64_t *keys_out, const DedupParams dd)
 {
     extern __shared__ uint64_t mlists[];  // [G][K]
     __shared__ uint64_t wl[kMergeWarps][32];
@@ -770,14 +894,30 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint
         if (ids_out) ids_out[o] = id;
         if (vals_out) vals_out[o] = v;
         if (keys_out) keys_out[o] = run;
+        if (dd.tab && id >= 0 && static_cast<int64_t>(id) < dd.V) {  // this candidate's gathered row
+            const int b = col / dd.L, t = col % dd.L;
+            const uint32_t gr = static_cast<uint32_t>(b * dd.R + 1 + t * dd.K + lane);
+            atomicMax(reinterpret_cast<unsigned long long *>(dd.tab + id),
+                      static_cast<unsigned long long>((static_cast<uint64_t>(dd.epoch) << 32) | ~gr));
+        }
     }
+    if (dd.tab && threadIdx.x == 32 && col % dd.L == 0) {  // the sequence's anchor row
+        const int b = col / dd.L;
+        int32_t x0 = dd.anchor[b];
+        if (x0 < 0 || static_cast<int64_t>(x0) >= dd.V) x0 = 0;  // reported by the compaction
+        const uint32_t gr = static_cast<uint32_t>(b * dd.R);
+        atomicMax(reinterpret_cast<unsigned long long *>(dd.tab + x0),
+                  static_cast<unsigned long long>((static_cast<uint64_t>(dd.epoch) << 32) | ~gr));
+    }
+    if (dd.tab && col == 0 && threadIdx.x == 64) *dd.count = 0;  // the compaction runs after this kernel
 }
 
 }  // namespace
 
-size_t lmhead_smem_bytes(int NT, int K, int stages, int boxes)
+size_t lmhead_smem_bytes(int NT, int K, int stages, int boxes, int hrows)
 {
-    return static_cast<size_t>(make_layout(NT, K, stages, boxes).total) + 1024;  // + alignment slack
+    return static_cast<size_t>(make_layout(NT, K, stages, boxes, hrows < 0 ? NT : hrows).total) +
+           1024;  // + alignment slack
 }
 
 int lmhead_boxes(int d, int NT)
@@ -795,22 +935,62 @@ int lmhead_boxes(int d, int NT)
 
 cudaError_t prepare_lmhead(int smem_optin)
 {
-    cudaError_t e = set_max_dynamic_smem(lmhead_topk_kernel, smem_optin);
+    cudaError_t e = set_max_dynamic_smem(lmhead_topk_kernel<false>, smem_optin);
+    if (e == cudaSuccess) e = set_max_dynamic_smem(lmhead_topk_kernel<true>, smem_optin);
     if (e != cudaSuccess) return e;
     return set_max_dynamic_smem(topk_merge_kernel, smem_optin);
 }
 
 cudaError_t launch_lmhead_topk(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s)
 {
-    return launch_ex(lmhead_topk_kernel, dim3(grid), dim3(kLmThreads), smem, s, 1, p);
+    return launch_ex(lmhead_topk_kernel<false>, dim3(grid), dim3(kLmThreads), smem, s, 1, p);
+}
+
+// CTA pairs along x (blockIdx.x 2i and 2i + 1 form pair i), PDL allowed.
+static cudaLaunchConfig_t pair_config(int grid, size_t smem, cudaStream_t s, cudaLaunchAttribute (&attr)[2])
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kLmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cfg;
+}
+
+cudaError_t launch_lmhead_topk_pair(const LmHeadParams &p, int grid, size_t smem, cudaStream_t s)
+{
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config(grid, smem, s, attr);
+    return cudaLaunchKernelEx(&cfg, lmhead_topk_kernel<true>, p);
+}
+
+int lmhead_pair_max_clusters(size_t smem)
+{
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_config(2, smem, nullptr, attr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, lmhead_topk_kernel<true>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws, float *vals_ws,
-                              int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s, uint64_t *keys_out)
+                              int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s, uint64_t *keys_out,
+                              const DedupParams &dd)
 {
     const size_t smem = static_cast<size_t>(G) * K * sizeof(uint64_t);
     return launch_ex(topk_merge_kernel, dim3(N), dim3(kMergeWarps * 32), smem, s, 1, part, G, N, K, ids_ws,
-                     vals_ws, ids_out, vals_out, thr_g, keys_out);
+                     vals_ws, ids_out, vals_out, thr_g, keys_out, dd);
 }
 
 }  // namespace dfl

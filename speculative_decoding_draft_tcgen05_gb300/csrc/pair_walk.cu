@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
     __shared__ float vals[K];
     __shared__ WalkSmem<K> ws;
     __shared__ int is_last;
+    __shared__ int32_t dd_row[2 * K];  // deduplicated AB rows of the predecessors and the candidates
 
     pdl_trigger();
     pdl_wait();
@@ -40,6 +41,23 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
     const int tid = threadIdx.x;
     const int n_prev = (t == 0) ? 1 : K;
     const size_t pos = static_cast<size_t>(b) * L + t;
+
+    if (p.dd_tab) {
+        if (tid < 2 * K && (tid < n_prev || tid >= K)) {
+            int32_t tok;
+            if (tid >= K) {
+                tok = p.ids[pos * K + (tid - K)];
+            } else if (t == 0) {
+                tok = p.anchor[b];
+                if (tok < 0 || static_cast<int64_t>(tok) >= p.V) tok = 0;  // reported by the compaction
+            } else {
+                tok = p.ids[(pos - 1) * K + tid];
+            }
+            const uint64_t mark = __ldcg(reinterpret_cast<const unsigned long long *>(p.dd_tab + tok));
+            dd_row[tid] = __ldcg(p.dd_rep + ~static_cast<uint32_t>(mark));
+        }
+        __syncthreads();
+    }
 
     {
         const int k = tid;  // blockDim.x == kEmbed: thread k owns component k
@@ -64,6 +82,12 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
             }
 #pragma unroll
             for (int j = 0; j < K; ++j) bb[j] = __ldg(p.tab + static_cast<size_t>(cur[j]) * 512 + kEmbed + k);
+        } else if (p.dd_tab) {
+#pragma unroll
+            for (int i = 0; i < K; ++i)
+                a[i] = (i < n_prev) ? p.AB[static_cast<size_t>(dd_row[i]) * 512 + k] : 0.f;
+#pragma unroll
+            for (int j = 0; j < K; ++j) bb[j] = p.AB[static_cast<size_t>(dd_row[K + j]) * 512 + kEmbed + k];
         } else {
 #pragma unroll
             for (int i = 0; i < K; ++i) a[i] = (i < n_prev) ? p.AB[(rowA0 + i) * 512 + k] : 0.f;

@@ -127,6 +127,15 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
     pdl_trigger();
+    // Deduplicated rows: their count comes from the previous kernel, so every
+    // role waits for it first; a tile past the count does no work.
+    int n_rows = p.R_total;
+    if (p.uniq) {
+        pdl_wait();
+        n_rows = static_cast<int>(*reinterpret_cast<const volatile unsigned *>(p.count));
+    }
+    const bool active = row0 < n_rows;
+    const int KBe = active ? KB : 0;
 
     bool timed_out = false;
     if (warp == 0) {
@@ -134,13 +143,13 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
         if (lane == 0) {
             tma_prefetch_desc(tmw);
             const uint64_t pol = l2_policy_evict_last();  // every row tile reads the same weights
-            const int pre = KB < kPrStages ? KB : kPrStages;
+            const int pre = KBe < kPrStages ? KBe : kPrStages;
             for (int kb = 0; kb < pre; ++kb) {  // weights: before the dependency wait
                 mbar_arrive_expect_tx(bar_full + 8u * kb, kPrWBytes);
                 tma_load_2d(base + kb * kPrStageBytes + kPrEBytes, tmw, (kb0 + kb) * 64, wrow0, bar_full + 8u * kb, pol);
             }
             int kb = pre;
-            for (; kb < KB; ++kb) {
+            for (; kb < KBe; ++kb) {
                 const int s = kb % kPrStages;
                 if (!mbar_wait(bar_empty + 8u * s, (static_cast<uint32_t>(kb / kPrStages) & 1u) ^ 1u, abort_flag)) {
                     timed_out = true;
@@ -158,7 +167,7 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kPrRows, NC);
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kb = 0; kb < KBe; ++kb) {
                 const int s = kb % kPrStages;
                 if (!mbar_wait(bar_full + 8u * s, static_cast<uint32_t>(kb / kPrStages) & 1u, abort_flag)) {
                     timed_out = true;
@@ -172,7 +181,10 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
                               idesc, (kb > 0 || k > 0) ? 1u : 0u);
                 umma_commit(bar_empty + 8u * s);  // frees the stage once these MMAs have read it
             }
-            umma_commit(bar_done);  // also after a timeout: every issued MMA must finish before TMEM is freed
+            if (active)
+                umma_commit(bar_done);  // also after a timeout: every issued MMA must finish before TMEM is freed
+            else
+                mbar_arrive(bar_done);  // no MMA was issued
         }
     } else {
         // ------------------------------------------------ gather the E rows
@@ -181,9 +193,10 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
         if (gt < kPrRows) {
             const int gr = row0 + gt;
             int32_t t = -1;
-            if (gr < p.R_total) {
+            if (gr < n_rows) {
                 const int b = gr / p.R, rr = gr % p.R;
-                t = (rr == 0) ? p.anchor[b] : p.ids[static_cast<size_t>(b) * p.L * p.K + (rr - 1)];
+                t = p.uniq ? p.uniq[gr]
+                           : ((rr == 0) ? p.anchor[b] : p.ids[static_cast<size_t>(b) * p.L * p.K + (rr - 1)]);
                 if (t < 0 || static_cast<int64_t>(t) >= p.V) {
                     atomicOr(p.err, DEV_ERR_TOKEN);
                     t = 0;
@@ -193,7 +206,7 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");  // the gathering warps only
         int arrived = 0;  // k-blocks this thread has signalled
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = 0; kb < KBe; ++kb) {
             const int s = kb % kPrStages;
             if (kb >= kPrStages &&
                 !mbar_wait(bar_empty + 8u * s, (static_cast<uint32_t>(kb / kPrStages) & 1u) ^ 1u, abort_flag)) {
@@ -220,14 +233,14 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
         cp_async_wait<0>();
         fence_proxy_async_smem();
         if (!timed_out)
-            for (; arrived < KB; ++arrived) mbar_arrive(bar_full + 8u * (arrived % kPrStages));
+            for (; arrived < KBe; ++arrived) mbar_arrive(bar_full + 8u * (arrived % kPrStages));
     }
     __syncwarp();
 
     // ---------------------------------------------------- epilogue: TMEM -> AB
     if (!mbar_wait(bar_done, 0, abort_flag, false)) timed_out = true;
     tc_fence_after_sync();
-    if (warp >= 2 && warp < 6) {
+    if (active && warp >= 2 && warp < 6) {
         const int q = warp & 3;  // warp w may read TMEM lanes 32 (w % 4) ..
         const int r = q * 32 + lane;
         const int gr = row0 + r;
@@ -238,7 +251,7 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
             float v[16];
             __syncwarp();
             tmem_load16(taddr + static_cast<uint32_t>(c0), v);
-            if (gr < p.R_total) {
+            if (gr < n_rows) {
 #pragma unroll
                 for (int j = 0; j < 16; j += 4)
                     *reinterpret_cast<float4 *>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
@@ -269,7 +282,7 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
             const size_t zstride = static_cast<size_t>(p.R_total) * 512;
             for (int e = threadIdx.x; e < kPrRows * nc4; e += kPrThreads) {
                 const int gr = row0 + e / nc4;
-                if (gr >= p.R_total) break;  // e grows with the row
+                if (gr >= n_rows) break;  // e grows with the row
                 const size_t off = static_cast<size_t>(gr) * 512 + ct * NC + (e % nc4) * 4;
                 float4 acc = __ldcg(reinterpret_cast<const float4 *>(p.part + off));
                 for (int z = 1; z < p.ksplit; ++z) {
@@ -282,6 +295,29 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
                 *reinterpret_cast<float4 *>(p.AB + off) = acc;
             }
         }
+    }
+}
+
+// One thread per gathered row: the row that holds the newest mark of its
+// token takes the next index of the distinct-token list.
+__global__ void __launch_bounds__(256) dedup_compact_kernel(const DedupParams d, const int32_t *__restrict__ ids,
+                                                            int R_total)
+{
+    pdl_trigger();
+    pdl_wait();
+    const int gr = blockIdx.x * blockDim.x + threadIdx.x;
+    if (gr >= R_total) return;
+    const int b = gr / d.R, rr = gr % d.R;
+    int32_t tok = (rr == 0) ? d.anchor[b] : ids[static_cast<size_t>(b) * d.L * d.K + (rr - 1)];
+    if (tok < 0 || static_cast<int64_t>(tok) >= d.V) {
+        atomicOr(d.err, DEV_ERR_TOKEN);
+        tok = 0;
+    }
+    const uint64_t mine = (static_cast<uint64_t>(d.epoch) << 32) | ~static_cast<uint32_t>(gr);
+    if (__ldcg(reinterpret_cast<const unsigned long long *>(d.tab + tok)) == mine) {
+        const unsigned u = atomicAdd(d.count, 1u);
+        d.uniq[u] = tok;
+        d.rep[gr] = static_cast<int32_t>(u);
     }
 }
 
@@ -325,6 +361,11 @@ int projection_cols(int R_total, int num_sms)
     if (8 * rt <= num_sms) return 64;
     if (4 * rt <= num_sms) return 128;
     return 256;
+}
+
+cudaError_t launch_dedup_compact(const DedupParams &d, const int32_t *ids, int R_total, cudaStream_t s)
+{
+    return launch_ex(dedup_compact_kernel, dim3((R_total + 255) / 256), dim3(256), 0, s, 1, d, ids, R_total);
 }
 
 cudaError_t launch_projection(const ProjParams &p, int NC, cudaStream_t s)

@@ -64,14 +64,15 @@ def to_device(inp: wl.Inputs, dev):
     return {k: getattr(inp, k).to(dev) for k in ("W", "E", "W_A", "W_B", "W_H", "hidden", "anchor")}
 
 
-def run_gpu(inp: wl.Inputs, dev="cuda", walk=0, max_batch=None, dtensors=None, targets=None, tables=False):
+def run_gpu(inp: wl.Inputs, dev="cuda", walk=0, max_batch=None, dtensors=None, targets=None, tables=False,
+            dedup=False):
     """Runs the whole selector through the C ABI (and, given target tokens
     [B, L+1], the accept check); returns CPU numpy outputs."""
     import speculative_decoding_draft_tcgen05_gb300 as pkg
     w = inp.wl
     d = dtensors if dtensors is not None else to_device(inp, dev)
     with pkg.Selector(d["W"], d["E"], d["W_A"], d["W_B"], d["W_H"], L=w.L, K=w.K,
-                      max_batch=max_batch or w.B, walk=walk, tie_eps=TIE_EPS, tables=tables) as sel:
+                      max_batch=max_batch or w.B, walk=walk, tie_eps=TIE_EPS, tables=tables, dedup=dedup) as sel:
         out = sel.run(d["hidden"], d["anchor"])
         if targets is not None:
             out["accept"] = torch.empty(w.B, dtype=torch.int32, device=dev)

@@ -65,6 +65,13 @@ EDGE = [
     dict(B=2, L=2, K=32, V=32, d=64),
     # one sequence, vocabulary just above one tile
     dict(B=1, L=5, K=16, V=129, d=256),
+    # 129 to 256 positions take the CTA-pair lm_head kernel: 200 positions (104
+    # per CTA), an odd vocabulary tile count (the pair's last tile is half past V)
+    dict(B=25, L=8, K=16, V=20000, d=128),
+    # 256 positions at K = 32 with the sampled-threshold pilot pass (258 tiles)
+    dict(B=16, L=16, K=32, V=33000, d=192),
+    # 135 positions (72 per CTA), odd tile count, pilot, d not a multiple of 128
+    dict(B=9, L=15, K=16, V=40000, d=320),
 ]
 
 
