@@ -113,6 +113,7 @@ constexpr int kProfileSlots = 5;    // launches recorded per run
 // position tile) seeds the thresholds of position tiles at least
 // DFL_LM_PILOT_MIN_NT wide.
 constexpr int kPilotTiles = 64;
+constexpr int kPilotMaxTiles = 160;  // maxima the main pass reads per position (5 per lane)
 #ifndef DFL_LM_PILOT_MIN_NT
 #define DFL_LM_PILOT_MIN_NT 96
 #endif
@@ -127,8 +128,10 @@ constexpr int kPilotTiles = 64;
 #ifndef DFL_LM_PAIR
 #define DFL_LM_PAIR 1
 #endif
+// Two 64-column boxes per stage (three stages of 60 KB rather than six of
+// 30 KB): measured 4b_b32 lm_head 191 -> 178 us.
 #ifndef DFL_LM_PAIR_BOXES
-#define DFL_LM_PAIR_BOXES 1
+#define DFL_LM_PAIR_BOXES 2
 #endif
 
 struct Plan {
@@ -136,7 +139,7 @@ struct Plan {
     bool pair;                    // the CTA-pair kernel (one position tile, G = 2 x pairs)
     int mt_vocab, mt_total;       // weight tiles of the pass (a pair: vocabulary tiles rounded up to even)
     int pilot_G, pilot_stride;  // pilot CTAs per position tile and their tile stride (0: no pilot)
-    int pilot_stages, pilot_boxes;
+    int pilot_NT, pilot_ntiles, pilot_stages, pilot_boxes;  // the pilot's own position tiling
     size_t pilot_smem;
     size_t smem;
     bool fused_tail;  // one clustered kernel for merge + projections + tables + walk
@@ -169,7 +172,7 @@ struct dflash_select_ctx {
     uint64_t *part = nullptr;
     uint64_t *thr_g = nullptr;  // per-position lm_head thresholds shared by the CTAs
     uint64_t *tmax = nullptr;   // [num_sms][max_batch * L] best logit of each lm_head CTA, epoch-tagged
-    uint64_t *pmax = nullptr;   // [kPilotTiles][max_batch * L] the pilot's tile maxima, epoch-tagged
+    uint64_t *pmax = nullptr;   // [kPilotMaxTiles][max_batch * L] the pilot's tile maxima, epoch-tagged
     uint32_t epoch = 0;
     float *gate = nullptr, *vals = nullptr, *AB = nullptr, *P = nullptr;
     float *tab = nullptr;  // [V][512] precomputed A|B of every token (cfg.tables)
@@ -247,18 +250,27 @@ struct dflash_select_ctx {
         p.smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, p.stages, p.boxes, hrows);
         p.pilot_G = 0;
         p.pilot_stride = 0;
+        p.pilot_NT = p.NT;
+        p.pilot_ntiles = p.n_tiles_n;
         p.pilot_boxes = p.boxes;
         p.pilot_stages = p.stages;
         p.pilot_smem = p.smem;
         if (p.NT >= DFL_LM_PILOT_MIN_NT && p.n_tiles_n <= DFL_LM_PILOT_MAX_NTILES &&
             m_tiles_vocab >= 4 * kPilotTiles) {
-            p.pilot_G = kPilotTiles;
-            p.pilot_stride = m_tiles_vocab / kPilotTiles;
-            if (p.pair) {  // the pilot runs the single-CTA kernel over the whole position tile
-                p.pilot_boxes = dfl::lmhead_boxes(cfg.d, p.NT);
-                p.pilot_stages = stages_for(p.NT, p.pilot_boxes, p.NT);
-                p.pilot_smem = dfl::lmhead_smem_bytes(p.NT, cfg.K, p.pilot_stages, p.pilot_boxes);
+            if (p.pair) {  // the pilot runs the single-CTA kernel on position tiles of at most 128
+                p.pilot_ntiles = (p.N + 127) / 128;
+                p.pilot_NT = ((p.N + p.pilot_ntiles - 1) / p.pilot_ntiles + 15) / 16 * 16;
+                p.pilot_boxes = dfl::lmhead_boxes(cfg.d, p.pilot_NT);
+                p.pilot_stages = stages_for(p.pilot_NT, p.pilot_boxes, p.pilot_NT);
+                p.pilot_smem = dfl::lmhead_smem_bytes(p.pilot_NT, cfg.K, p.pilot_stages, p.pilot_boxes);
             }
+            // one wave of CTAs, at least kPilotTiles sampled tiles per position tile
+            int g = num_sms / p.pilot_ntiles;
+            if (g < kPilotTiles) g = kPilotTiles;
+            if (g > kPilotMaxTiles) g = kPilotMaxTiles;
+            if (g > m_tiles_vocab / 4) g = m_tiles_vocab / 4;
+            p.pilot_G = g;
+            p.pilot_stride = m_tiles_vocab / g;
         }
         p.R_total = B * R;
         p.tail_cs = dfl::tail_cluster_size(cfg.d);
@@ -416,7 +428,7 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     const size_t o_part = off; off += up(part_elems * 8);
     const size_t o_thrg = off; off += up(Nmax * 8);
     const size_t o_tmax = off; off += up(static_cast<size_t>(prop.multiProcessorCount) * Nmax * 8);
-    const size_t o_pmax = off; off += up(static_cast<size_t>(kPilotTiles) * Nmax * 8);
+    const size_t o_pmax = off; off += up(static_cast<size_t>(kPilotMaxTiles) * Nmax * 8);
     const size_t o_gate = off; off += up(Nmax * dfl::kEmbed * 4);
     const size_t o_ids = off; off += up(Nmax * cfg->K * 4);
     const size_t o_vals = off; off += up(Nmax * cfg->K * 4);
@@ -562,12 +574,12 @@ static dflash_status launch_lmhead(dflash_select_ctx *c, const void *hidden, con
         c->h_rows = pl.N;
         c->h_box = box;
     }
-    if (pl.pair && pl.pilot_G > 0 && (hidden != c->hp_ptr || pl.N != c->hp_rows || pl.NT != c->hp_box)) {
-        dflash_status st = make_tmap(&c->tm_hp, hidden, pl.N, c->cfg.d, pl.NT);
+    if (pl.pair && pl.pilot_G > 0 && (hidden != c->hp_ptr || pl.N != c->hp_rows || pl.pilot_NT != c->hp_box)) {
+        dflash_status st = make_tmap(&c->tm_hp, hidden, pl.N, c->cfg.d, pl.pilot_NT);
         if (st != DFLASH_OK) return st;
         c->hp_ptr = hidden;
         c->hp_rows = pl.N;
-        c->hp_box = pl.NT;
+        c->hp_box = pl.pilot_NT;
     }
     dfl::LmHeadParams lp;
     lp.tm_w = c->tm_w;
@@ -602,10 +614,12 @@ static dflash_status launch_lmhead(dflash_select_ctx *c, const void *hidden, con
         pp.m_tiles_total = c->m_tiles_total;
         pp.stages = pl.pilot_stages;
         pp.boxes = pl.pilot_boxes;
+        pp.NT = pl.pilot_NT;
+        pp.n_tiles_n = pl.pilot_ntiles;
         if (pl.pair) pp.tm_h = c->tm_hp;
         pp.tmax = nullptr;
         pp.pmax = c->pmax;
-        CUDA_TRY(dfl::launch_lmhead_topk(pp, pl.pilot_G * pl.n_tiles_n, pl.pilot_smem, s));
+        CUDA_TRY(dfl::launch_lmhead_topk(pp, pl.pilot_G * pl.pilot_ntiles, pl.pilot_smem, s));
         lp.tmax = nullptr;  // the pilot's maxima replace the CTAs' own
         lp.pmax = c->pmax;
         lp.pmax_n = pl.pilot_G;

@@ -35,6 +35,10 @@ constexpr uint32_t kTransposeBytes = 16 * kLmTileM * 4;    // 16 columns x 128 r
 constexpr int kInsertLimit = 6;
 // Keys the per-tile path can hold per tile (buckets over the transpose buffer).
 constexpr int kBucketKeys = static_cast<int>(kTransposeBytes / 8);
+// Survivors beyond a position's bucket go to a small pool shared by all
+// positions (over the chunked path's row scratch, which the per-tile path does
+// not use); only a full pool sends the tile through the chunked path.
+constexpr int kPoolKeys = 64;
 // First tile (per CTA) that takes the per-tile path. Nearly every logit of
 // the first tile passes (the lists are empty), and many of the second at 100+
 // positions (more than the buckets hold): both go through the chunked path.
@@ -227,6 +231,9 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     uint64_t *const bucket = reinterpret_cast<uint64_t *>(T);
     uint32_t *const col_cnt = reinterpret_cast<uint32_t *>(gbase + lay.off_ccnt);
     volatile uint32_t *const ovf = chunk_flags + 4;
+    uint64_t *const pool_key = reinterpret_cast<uint64_t *>(wscr);                  // [kPoolKeys]
+    uint16_t *const pool_col = reinterpret_cast<uint16_t *>(wscr + 8 * kPoolKeys);  // [kPoolKeys]
+    volatile uint32_t *const pool_cnt = chunk_flags + 6;                            // per tile parity
     const uint32_t bar_full = base + lay.off_bar;
     const uint32_t bar_empty = bar_full + 8u * S;
     const uint32_t bar_tfull = bar_empty + 8u * S;
@@ -471,7 +478,10 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
             const bool gate = m >= p.m_tiles_vocab;
             // the overflow flag of the next tile: every thread read it (as the
             // flag of tile j - 1) before the barriers that ended that tile
-            if (threadIdx.x == 64) ovf[(j + 1) & 1] = 0;
+            if (threadIdx.x == 64) {
+                ovf[(j + 1) & 1] = 0;
+                pool_cnt[(j + 1) & 1] = 0;
+            }
             // the cross-CTA thresholds, fetched while the accumulator fills
             uint64_t tg[2] = {0ull, 0ull};
             if (!gate) {
@@ -615,10 +625,18 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                             pm &= pm - 1;
                             const int col = c0 + jj;
                             const uint32_t slot = atomicAdd(col_cnt + col, 1u);
-                            if (slot < static_cast<uint32_t>(capc))
-                                bucket[slot * NT + col] = make_key(pick16(v, jj), p.id_base + static_cast<uint32_t>(row0 + row));
-                            else
-                                ovf[j & 1] = 1;
+                            const uint64_t key = make_key(pick16(v, jj), p.id_base + static_cast<uint32_t>(row0 + row));
+                            if (slot < static_cast<uint32_t>(capc)) {
+                                bucket[slot * NT + col] = key;
+                            } else {
+                                const uint32_t ps = atomicAdd(const_cast<uint32_t *>(&pool_cnt[j & 1]), 1u);
+                                if (ps < static_cast<uint32_t>(kPoolKeys)) {
+                                    pool_key[ps] = key;
+                                    pool_col[ps] = static_cast<uint16_t>(col);
+                                } else {
+                                    ovf[j & 1] = 1;
+                                }
+                            }
                         }
                     }
                 }
@@ -635,9 +653,17 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
                     if (nsurv > 0) {  // thread et owns position et
                         const int c = et;
                         uint64_t th = thr[c], kth = 0;
-                        const bool dirty =
-                            K == 16 ? insert_into_list<16>(lists + c, LS, bucket + c, NT, nsurv, th, kth)
-                                    : insert_into_list<32>(lists + c, LS, bucket + c, NT, nsurv, th, kth);
+                        const int nb = nsurv < capc ? nsurv : capc;
+                        bool dirty = K == 16 ? insert_into_list<16>(lists + c, LS, bucket + c, NT, nb, th, kth)
+                                             : insert_into_list<32>(lists + c, LS, bucket + c, NT, nb, th, kth);
+                        if (nsurv > capc) {  // the rest of this position's survivors are in the pool
+                            const uint32_t np = pool_cnt[j & 1];
+                            for (uint32_t i = 0; i < np; ++i) {
+                                if (pool_col[i] != c) continue;
+                                dirty |= K == 16 ? insert_into_list<16>(lists + c, LS, pool_key + i, 1, 1, th, kth)
+                                                 : insert_into_list<32>(lists + c, LS, pool_key + i, 1, 1, th, kth);
+                            }
+                        }
                         if (dirty) {
                             thr[c] = th;
                             thr_f[c] = th ? key_val(th) : -INFINITY;
@@ -840,6 +866,7 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
 // them into a sorted list, then the warps' lists are folded pairwise in a
 // tree (4 rounds).
 constexpr int kMergeWarps = 16;
+constexpr int kMergeSurvivors = 128;  // keys the fast path sorts (four warp-wide batches)
 
 __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint64_t *__restrict__ part, int G,
                                                                       int N, int K, int32_t *ids_ws,
@@ -871,19 +898,59 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint
         }
     }
     __syncthreads();
-    uint64_t run = 0;
-    for (int g = warp; g < G; g += kMergeWarps) {
-        const uint64_t x = (lane < K) ? mlists[g * K + lane] : 0ull;
-        run = list_merge(run, x, lane, K);
-    }
-    wl[warp][lane] = run;
-    __syncthreads();
-    for (int step = 1; step < kMergeWarps; step <<= 1) {
-        if ((warp & (2 * step - 1)) == 0) {
-            run = list_merge(run, wl[warp + step][lane], lane, K);
-            wl[warp][lane] = run;
+    // Fast path: K lists whose best keys are all >= v hold K keys >= v, so v
+    // (the K-th largest of the lanes' best list heads) bounds the K-th best key
+    // from below and only keys >= v can be in the result. Usually a few dozen
+    // pass; they are sorted by one warp. With more (or fewer than K lists) the
+    // lists are merged whole.
+    __shared__ uint64_t bound_s;
+    __shared__ unsigned nsurv_s;
+    __shared__ uint64_t surv[kMergeSurvivors];
+    if (warp == 0) {
+        uint64_t best = 0;
+        for (int g = lane; g < G; g += 32) best = mlists[g * K] > best ? mlists[g * K] : best;
+        best = warp_sort_desc(best, lane);
+        const uint64_t v = shfl_u64(best, K - 1);
+        if (lane == 0) {
+            bound_s = v;
+            nsurv_s = 0;
         }
+    }
+    __syncthreads();
+    const uint64_t bound = bound_s;
+    if (bound != 0) {
+        for (int i = threadIdx.x; i < G * K; i += kMergeWarps * 32) {
+            const uint64_t x = mlists[i];
+            if (x >= bound) {
+                const unsigned slot = atomicAdd(&nsurv_s, 1u);
+                if (slot < kMergeSurvivors) surv[slot] = x;
+            }
+        }
+    }
+    __syncthreads();
+    const unsigned ns = nsurv_s;
+    uint64_t run = 0;
+    if (bound != 0 && ns <= kMergeSurvivors) {
+        if (warp == 0) {
+            for (unsigned b0 = 0; b0 < ns; b0 += 32) {
+                const uint64_t x = (b0 + lane < ns) ? surv[b0 + lane] : 0ull;
+                run = list_merge(run, warp_sort_desc(x, lane), lane, K);
+            }
+        }
+    } else {
+        for (int g = warp; g < G; g += kMergeWarps) {
+            const uint64_t x = (lane < K) ? mlists[g * K + lane] : 0ull;
+            run = list_merge(run, x, lane, K);
+        }
+        wl[warp][lane] = run;
         __syncthreads();
+        for (int step = 1; step < kMergeWarps; step <<= 1) {
+            if ((warp & (2 * step - 1)) == 0) {
+                run = list_merge(run, wl[warp + step][lane], lane, K);
+                wl[warp][lane] = run;
+            }
+            __syncthreads();
+        }
     }
     if (warp == 0 && lane < K) {
         const int32_t id = key_id(run);
