@@ -205,10 +205,13 @@ struct dflash_select_ctx {
 #ifndef DFL_LM_TILE_POS
 #define DFL_LM_TILE_POS 128
 #endif
-        p.pair = DFL_LM_PAIR && p.N > 128 && p.N <= 256 && pair_clusters > 0;
+        p.pair = DFL_LM_PAIR && p.N > 128 && pair_clusters > 0;
+        if (p.pair) {  // position tiles of up to 256, half of each in either CTA of a pair
+            p.n_tiles_n = (p.N + 255) / 256;
+            p.NT = ((p.N + p.n_tiles_n - 1) / p.n_tiles_n + 15) / 16 * 16;
+            if (pair_clusters < p.n_tiles_n) p.pair = false;
+        }
         if (p.pair) {
-            p.n_tiles_n = 1;
-            p.NT = (p.N + 15) / 16 * 16;
         } else if (p.N <= 256) {
             p.n_tiles_n = (p.N + DFL_LM_TILE_POS - 1) / DFL_LM_TILE_POS;
             p.NT = (((p.N + p.n_tiles_n - 1) / p.n_tiles_n) + 15) / 16 * 16;
@@ -230,14 +233,16 @@ struct dflash_select_ctx {
         };
         int hrows = p.NT;
         if (p.pair) {
-            int g2 = num_sms / 2;
-            if (g2 > pair_clusters) g2 = pair_clusters;
+            int g2 = (num_sms / 2) / p.n_tiles_n;  // pairs per position tile
+            if (g2 > pair_clusters / p.n_tiles_n) g2 = pair_clusters / p.n_tiles_n;
             if (g2 > p.mt_total / 2) g2 = p.mt_total / 2;
             p.G = 2 * g2;
-            p.grid = 2 * g2;
-            p.boxes = DFL_LM_PAIR_BOXES;
-            while (p.boxes > 1 && cfg.d % (dfl::kLmTileK * p.boxes) != 0) --p.boxes;
+            p.grid = 2 * g2 * p.n_tiles_n;
             hrows = p.NT / 2;
+            // two boxes per stage where three such stages fit, else one
+            p.boxes = DFL_LM_PAIR_BOXES;
+            while (p.boxes > 1 && (cfg.d % (dfl::kLmTileK * p.boxes) != 0 || stages_for(p.NT, p.boxes, hrows) < 3))
+                --p.boxes;
         } else {
             int g = num_sms / p.n_tiles_n;
             if (g < 1) g = 1;
@@ -257,16 +262,19 @@ struct dflash_select_ctx {
         p.pilot_smem = p.smem;
         if (p.NT >= DFL_LM_PILOT_MIN_NT && p.n_tiles_n <= DFL_LM_PILOT_MAX_NTILES &&
             m_tiles_vocab >= 4 * kPilotTiles) {
-            if (p.pair) {  // the pilot runs the single-CTA kernel on position tiles of at most 128
-                p.pilot_ntiles = (p.N + 127) / 128;
-                p.pilot_NT = ((p.N + p.pilot_ntiles - 1) / p.pilot_ntiles + 15) / 16 * 16;
+            if (p.pair) {  // the pilot runs the single-CTA kernel (up to 256 positions: tiles of at most 128)
+                if (p.N <= 256) {
+                    p.pilot_ntiles = (p.N + 127) / 128;
+                    p.pilot_NT = ((p.N + p.pilot_ntiles - 1) / p.pilot_ntiles + 15) / 16 * 16;
+                }
                 p.pilot_boxes = dfl::lmhead_boxes(cfg.d, p.pilot_NT);
                 p.pilot_stages = stages_for(p.pilot_NT, p.pilot_boxes, p.pilot_NT);
                 p.pilot_smem = dfl::lmhead_smem_bytes(p.pilot_NT, cfg.K, p.pilot_stages, p.pilot_boxes);
             }
-            // one wave of CTAs, at least kPilotTiles sampled tiles per position tile
+            // one wave of CTAs with at least kPilotTiles sampled tiles per position tile; with many
+            // position tiles 2K of them (the bound takes the K-th largest of 32 lanes' maxima)
             int g = num_sms / p.pilot_ntiles;
-            if (g < kPilotTiles) g = kPilotTiles;
+            if (g < kPilotTiles) g = p.pilot_ntiles > 2 ? 2 * cfg.K : kPilotTiles;
             if (g > kPilotMaxTiles) g = kPilotMaxTiles;
             if (g > m_tiles_vocab / 4) g = m_tiles_vocab / 4;
             p.pilot_G = g;

@@ -243,8 +243,11 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tile = blockIdx.x % p.n_tiles_n;
-    const int chunk = blockIdx.x / p.n_tiles_n;
+    // a pair (CTAs 2i, 2i + 1) shares its position tile; chunk = the CTA's index
+    // among the CTAs of its position tile (its partial lists' slot)
+    const int n_tile = kPair ? static_cast<int>(blockIdx.x >> 1) % p.n_tiles_n : blockIdx.x % p.n_tiles_n;
+    const int chunk = kPair ? (static_cast<int>(blockIdx.x >> 1) / p.n_tiles_n) * 2 + static_cast<int>(blockIdx.x & 1)
+                            : blockIdx.x / p.n_tiles_n;
     const int G = p.ctas_per_ntile;
     const bool pilot = !kPair && p.pilot_stride > 0;
     // this CTA's tiles: chunk, chunk + G, ... (a pilot CTA: chunk * pilot_stride
