@@ -864,6 +864,39 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_topk_kernel(const __grid
     }
 }
 
+// Writes the merged list of position col (lanes 0..K-1 of one warp hold it)
+// and, with deduplication, marks its candidates' gathered rows (and, at a
+// sequence's first position, the anchor's, from the thread with first_thread).
+__device__ __forceinline__ void merge_emit(int col, uint64_t run, int lane, int K, int32_t *ids_ws, float *vals_ws,
+                                           int32_t *ids_out, float *vals_out, uint64_t *keys_out,
+                                           const DedupParams &dd, bool first_thread)
+{
+    if (lane < K) {
+        const int32_t id = key_id(run);
+        const float v = key_val(run);
+        const size_t o = static_cast<size_t>(col) * K + lane;
+        ids_ws[o] = id;
+        vals_ws[o] = v;
+        if (ids_out) ids_out[o] = id;
+        if (vals_out) vals_out[o] = v;
+        if (keys_out) keys_out[o] = run;
+        if (dd.tab && id >= 0 && static_cast<int64_t>(id) < dd.V) {  // this candidate's gathered row
+            const int b = col / dd.L, t = col % dd.L;
+            const uint32_t gr = static_cast<uint32_t>(b * dd.R + 1 + t * dd.K + lane);
+            atomicMax(reinterpret_cast<unsigned long long *>(dd.tab + id),
+                      static_cast<unsigned long long>((static_cast<uint64_t>(dd.epoch) << 32) | ~gr));
+        }
+    }
+    if (dd.tab && first_thread && col % dd.L == 0) {  // the sequence's anchor row
+        const int b = col / dd.L;
+        int32_t x0 = dd.anchor[b];
+        if (x0 < 0 || static_cast<int64_t>(x0) >= dd.V) x0 = 0;  // reported by the compaction
+        const uint32_t gr = static_cast<uint32_t>(b * dd.R);
+        atomicMax(reinterpret_cast<unsigned long long *>(dd.tab + x0),
+                  static_cast<unsigned long long>((static_cast<uint64_t>(dd.epoch) << 32) | ~gr));
+    }
+}
+
 // One CTA per position. The G partial lists of the position are staged in
 // shared memory with coalesced loads; each of the 16 warps folds a share of
 // them into a sorted list, then the warps' lists are folded pairwise in a
@@ -955,31 +988,33 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint
             __syncthreads();
         }
     }
-    if (warp == 0 && lane < K) {
-        const int32_t id = key_id(run);
-        const float v = key_val(run);
-        const size_t o = static_cast<size_t>(col) * K + lane;
-        ids_ws[o] = id;
-        vals_ws[o] = v;
-        if (ids_out) ids_out[o] = id;
-        if (vals_out) vals_out[o] = v;
-        if (keys_out) keys_out[o] = run;
-        if (dd.tab && id >= 0 && static_cast<int64_t>(id) < dd.V) {  // this candidate's gathered row
-            const int b = col / dd.L, t = col % dd.L;
-            const uint32_t gr = static_cast<uint32_t>(b * dd.R + 1 + t * dd.K + lane);
-            atomicMax(reinterpret_cast<unsigned long long *>(dd.tab + id),
-                      static_cast<unsigned long long>((static_cast<uint64_t>(dd.epoch) << 32) | ~gr));
-        }
-    }
-    if (dd.tab && threadIdx.x == 32 && col % dd.L == 0) {  // the sequence's anchor row
-        const int b = col / dd.L;
-        int32_t x0 = dd.anchor[b];
-        if (x0 < 0 || static_cast<int64_t>(x0) >= dd.V) x0 = 0;  // reported by the compaction
-        const uint32_t gr = static_cast<uint32_t>(b * dd.R);
-        atomicMax(reinterpret_cast<unsigned long long *>(dd.tab + x0),
-                  static_cast<unsigned long long>((static_cast<uint64_t>(dd.epoch) << 32) | ~gr));
-    }
+    if (warp == 0) merge_emit(col, run, lane, K, ids_ws, vals_ws, ids_out, vals_out, keys_out, dd, threadIdx.x == 0);
     if (dd.tab && col == 0 && threadIdx.x == 64) *dd.count = 0;  // the compaction runs after this kernel
+}
+
+// Few lists per position (G <= 32, e.g. the 10 CTAs of a 256-wide tile at
+// the stress shape, or a few vocabulary shards): one warp per position folds
+// the G lists in order, sixteen positions per CTA.
+__global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_small_kernel(
+    const uint64_t *__restrict__ part, int G, int N, int K, int32_t *ids_ws, float *vals_ws, int32_t *ids_out,
+    float *vals_out, uint64_t *thr_g, uint64_t *keys_out, const DedupParams dd)
+{
+    pdl_trigger();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int col = blockIdx.x * kMergeWarps + warp;
+    if (dd.tab && blockIdx.x == 0 && threadIdx.x == 0) *dd.count = 0;  // the compaction runs after this kernel
+    if (col >= N) return;
+    if (lane == 0) thr_g[col] = 0;  // ready for the next lm_head pass
+    uint64_t x[32];
+#pragma unroll
+    for (int g = 0; g < 32; ++g)  // every load issued before the first merge
+        x[g] = (g < G && lane < K) ? part[(static_cast<size_t>(g) * N + col) * K + lane] : 0ull;
+    uint64_t run = 0;
+#pragma unroll
+    for (int g = 0; g < 32; ++g)
+        if (g < G) run = list_merge(run, x[g], lane, K);
+    merge_emit(col, run, lane, K, ids_ws, vals_ws, ids_out, vals_out, keys_out, dd, lane == 0);
 }
 
 }  // namespace
@@ -1058,6 +1093,9 @@ cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t
                               int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s, uint64_t *keys_out,
                               const DedupParams &dd)
 {
+    if (G <= 32)
+        return launch_ex(topk_merge_small_kernel, dim3((N + kMergeWarps - 1) / kMergeWarps), dim3(kMergeWarps * 32), 0,
+                         s, 1, part, G, N, K, ids_ws, vals_ws, ids_out, vals_out, thr_g, keys_out, dd);
     const size_t smem = static_cast<size_t>(G) * K * sizeof(uint64_t);
     return launch_ex(topk_merge_kernel, dim3(N), dim3(kMergeWarps * 32), smem, s, 1, part, G, N, K, ids_ws,
                      vals_ws, ids_out, vals_out, thr_g, keys_out, dd);
