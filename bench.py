@@ -2,7 +2,8 @@
 
 One step = one pass of the whole selector (lm_head + top-K, merge,
 projections, pair tables + walk) and the greedy accept check over one batch
-of seeded synthetic inputs already resident in HBM. Prints one JSON line.
+of seeded synthetic inputs already resident in HBM (one
+dflash_select_run_verify call). Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4b_b1]
   python bench.py --impl reference ...   # the CPU oracle on the same workload
@@ -462,7 +463,8 @@ def run_ours(args):
     h2d = hid_h.numel() * 2 + anc_h.numel() * 4 + tgt_h.numel() * 4
     d2h = path_h.numel() * 4 + acc_h.numel() * 4 + em_h.numel() * 4 + 4
 
-    launches_per_step = pkg.dflash_select_launches_per_run(sel.h, w.B) + 1
+    # the step is one dflash_select_run_verify call: the accept check runs in the walking kernel
+    launches_per_step = pkg.dflash_select_launches_per_run(sel.h, w.B)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     N, NT, n_tiles, G = lmhead_geometry(w, sms)
     distinct = None

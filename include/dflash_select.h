@@ -164,10 +164,23 @@ dflash_status dflash_verify_rejection(const int32_t *path, const int32_t *topk_i
 dflash_status dflash_verify_prefix(const int32_t *path, const int32_t *target, int32_t B, int32_t L,
                                    int32_t *accept_len, int32_t *emitted, void *stream);
 
+/* dflash_select_run and dflash_verify_prefix in one call: the kernel that
+ * walks a sequence's tables also checks its path against the target tokens
+ * (one launch fewer per step). Same results as the two calls.
+ *   target     [B, L+1] int32  target argmax token after x0, path[0], ..., path[L-1]
+ *   path       [B, L] int32    draft tokens (output)
+ *   accept_len [B] int32       n = number of leading t with path[t] == target[t]
+ *   emitted    [B, L+1] int32  path[0..n-1], target[n], then -1 (NULL = not wanted)
+ *   topk_ids, topk_vals, pair_scores, path_score, tie_flags: as dflash_select_run
+ * Max-sum and greedy walks. Errors: as dflash_select_run. */
+dflash_status dflash_select_run_verify(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,
+                                       const int32_t *target, int32_t *path, int32_t *accept_len, int32_t *emitted,
+                                       int32_t *topk_ids, float *topk_vals, float *pair_scores, float *path_score,
+                                       uint8_t *tie_flags, void *stream);
+
 /* One whole draft-verify step from HOST buffers: copies hidden/anchor/target
- * to the handle's device staging area, runs dflash_select_run and
- * dflash_verify_prefix, copies path, accept_len and emitted back, and waits
- * for the stream. Host buffers should be pinned for asynchronous copies.
+ * to the handle's device staging area, runs dflash_select_run_verify, copies
+ * path, accept_len and emitted back, and waits for the stream. Host buffers should be pinned for asynchronous copies.
  *   hidden_host [B, L, d] bf16, anchor_host [B], target_host [B, L+1] int32
  *   path_host [B, L], accept_host [B], emitted_host [B, L+1] int32 (outputs)
  * Returns the same errors as the two calls, and any latched device error. */

@@ -77,6 +77,7 @@ def lib() -> ctypes.CDLL:
                                                    ctypes.POINTER(P)]
             L.dflash_select_topk_shard.argtypes = [P, P, i32, P, P]
             L.dflash_select_run_gathered.argtypes = [P, P, i32, P, i32, P, P, P, P, P, P, P]
+            L.dflash_select_run_verify.argtypes = [P, P, P, i32, P, P, P, P, P, P, P, P, P, P]
             L.dflash_lmhead_topk_noalloc.argtypes = [P, i64, i32, P, i32, i32, P, P, P, P]
             L.dflash_selftest_wait_timeout.argtypes = [P, P]
             L.dflash_conv2_init.argtypes = [P, P, i32, ctypes.POINTER(P)]
@@ -89,7 +90,7 @@ def lib() -> ctypes.CDLL:
                       "dflash_select_destroy", "dflash_lmhead_topk_noalloc", "dflash_select_run_sampled",
                       "dflash_verify_rejection", "dflash_conv2_init", "dflash_conv2_run", "dflash_conv2_sync_status",
                       "dflash_conv2_destroy", "dflash_selftest_wait_timeout", "dflash_select_init_shard",
-                      "dflash_select_topk_shard", "dflash_select_run_gathered"):
+                      "dflash_select_topk_shard", "dflash_select_run_gathered", "dflash_select_run_verify"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -204,6 +205,24 @@ def dflash_select_run(handle, hidden, anchor, *, path, topk_ids=None, topk_vals=
                                    _ptr(tie_flags, torch.uint8, "tie_flags"), _stream(stream)), "dflash_select_run")
 
 
+def dflash_select_run_verify(handle, hidden, anchor, target, *, path, accept_len, emitted=None, topk_ids=None,
+                             topk_vals=None, pair_scores=None, path_score=None, tie_flags=None, stream=None):
+    """dflash_select_run and dflash_verify_prefix in one call: target [B, L+1] int32 in, path [B, L],
+    accept_len [B] and emitted [B, L+1] out (the walking kernel checks the path)."""
+    import torch
+    B = anchor.shape[0]
+    _check(lib().dflash_select_run_verify(handle, _ptr(hidden, torch.bfloat16, "hidden"),
+                                          _ptr(anchor, torch.int32, "anchor"), B, _ptr(target, torch.int32, "target"),
+                                          _ptr(path, torch.int32, "path"), _ptr(accept_len, torch.int32, "accept_len"),
+                                          _ptr(emitted, torch.int32, "emitted"),
+                                          _ptr(topk_ids, torch.int32, "topk_ids"),
+                                          _ptr(topk_vals, torch.float32, "topk_vals"),
+                                          _ptr(pair_scores, torch.float32, "pair_scores"),
+                                          _ptr(path_score, torch.float32, "path_score"),
+                                          _ptr(tie_flags, torch.uint8, "tie_flags"), _stream(stream)),
+           "dflash_select_run_verify")
+
+
 def dflash_select_run_sampled(handle, hidden, anchor, u_walk, *, path, draft_probs, topk_ids=None, topk_vals=None,
                               pair_scores=None, path_score=None, tie_flags=None, stream=None):
     """The selector with the sampling walk: u_walk [B, L] fp32 uniforms in, draft_probs [B, L, K] out."""
@@ -285,9 +304,10 @@ def dflash_select_launches_per_run(handle, B: int) -> int:
 
 
 def bind_step(handle, hidden, anchor, path, target=None, accept_len=None, emitted=None, stream=None, **outs):
-    """Marshals the arguments of dflash_select_run (and, with target given,
-    dflash_verify_prefix) once and returns a zero-argument callable that makes
-    the same call(s) again; for tight loops over fixed buffers."""
+    """Marshals the arguments of dflash_select_run (with target given,
+    dflash_select_run_verify: the run and the accept check in one call) once and
+    returns a zero-argument callable that makes the same call again; for tight
+    loops over fixed buffers."""
     import torch
     L_ = lib()
     B = anchor.shape[0]
@@ -304,17 +324,21 @@ def bind_step(handle, hidden, anchor, path, target=None, accept_len=None, emitte
             if st:
                 _check(st, "dflash_select_run")
         return step
-    ver_args = (_ptr(path, torch.int32, "path"), _ptr(target, torch.int32, "target"), B, path.shape[1],
-                _ptr(accept_len, torch.int32, "accept_len"), _ptr(emitted, torch.int32, "emitted"), _stream(stream))
-    ver = L_.dflash_verify_prefix
+    # with targets: the fused run + accept check (one launch fewer than the two calls)
+    rv_args = (handle, _ptr(hidden, torch.bfloat16, "hidden"), _ptr(anchor, torch.int32, "anchor"), B,
+               _ptr(target, torch.int32, "target"), _ptr(path, torch.int32, "path"),
+               _ptr(accept_len, torch.int32, "accept_len"), _ptr(emitted, torch.int32, "emitted"),
+               _ptr(outs.get("topk_ids"), torch.int32, "topk_ids"),
+               _ptr(outs.get("topk_vals"), torch.float32, "topk_vals"),
+               _ptr(outs.get("pair_scores"), torch.float32, "pair_scores"),
+               _ptr(outs.get("path_score"), torch.float32, "path_score"),
+               _ptr(outs.get("tie_flags"), torch.uint8, "tie_flags"), _stream(stream))
+    rv = L_.dflash_select_run_verify
 
     def step():
-        st = run(*run_args)
+        st = rv(*rv_args)
         if st:
-            _check(st, "dflash_select_run")
-        st = ver(*ver_args)
-        if st:
-            _check(st, "dflash_verify_prefix")
+            _check(st, "dflash_select_run_verify")
     return step
 
 

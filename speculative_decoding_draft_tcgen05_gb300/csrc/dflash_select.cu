@@ -646,7 +646,9 @@ static dflash_status launch_lmhead(dflash_select_ctx *c, const void *hidden, con
 static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, int32_t B, const Plan &pl,
                                  const uint64_t *part, int G, const float *u_walk, int32_t *topk_ids,
                                  float *topk_vals, float *pair_scores, int32_t *path, float *draft_probs,
-                                 float *path_score, uint8_t *tie_flags, cudaStream_t s)
+                                 float *path_score, uint8_t *tie_flags, cudaStream_t s,
+                                 const int32_t *target = nullptr, int32_t *accept = nullptr,
+                                 int32_t *emitted = nullptr)
 {
     int tail_S = pl.tail_S;
     size_t tail_smem = pl.tail_smem;
@@ -688,6 +690,9 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
         tp.u_walk = u_walk;
         tp.q_out = draft_probs;
         tp.temperature = c->cfg.temperature;
+        tp.target = target;
+        tp.accept = accept;
+        tp.emitted = emitted;
         prof_begin(c, 1, s);
         CUDA_TRY(dfl::launch_select_tail(tp, c->cfg.K, tail_S, tail_smem, s));
         prof_end(c, 1, 4, s);
@@ -778,6 +783,9 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
         q.dd_tab = c->dd_tab;
         q.dd_rep = c->dd_rep;
     }
+    q.target = target;
+    q.accept = accept;
+    q.emitted = emitted;
     prof_begin(c, slot, s);
     CUDA_TRY(dfl::launch_pair_walk(q, s));
     prof_end(c, slot, 3, s);
@@ -788,7 +796,8 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
 static dflash_status run_impl(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,
                               const float *u_walk, int32_t *topk_ids, float *topk_vals, float *pair_scores,
                               int32_t *path, float *draft_probs, float *path_score, uint8_t *tie_flags,
-                              void *stream)
+                              void *stream, const int32_t *target = nullptr, int32_t *accept = nullptr,
+                              int32_t *emitted = nullptr)
 {
     if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is NULL");
     dflash_select_ctx *c = h;
@@ -805,7 +814,7 @@ static dflash_status run_impl(dflash_select_handle h, const void *hidden, const 
     dflash_status st = launch_lmhead(c, hidden, pl, s);
     if (st != DFLASH_OK) return st;
     return launch_tail(c, anchor, B, pl, c->part, pl.G, u_walk, topk_ids, topk_vals, pair_scores, path, draft_probs,
-                       path_score, tie_flags, s);
+                       path_score, tie_flags, s, target, accept, emitted);
 }
 
 dflash_status dflash_select_topk_shard(dflash_select_handle h, const void *hidden, int32_t B, uint64_t *shard_keys,
@@ -861,6 +870,18 @@ dflash_status dflash_select_run(dflash_select_handle h, const void *hidden, cons
         return fail(DFLASH_ERR_INVALID_ARG, "a sampling handle runs through dflash_select_run_sampled");
     return run_impl(h, hidden, anchor, B, nullptr, topk_ids, topk_vals, pair_scores, path, nullptr, path_score,
                     tie_flags, stream);
+}
+
+dflash_status dflash_select_run_verify(dflash_select_handle h, const void *hidden, const int32_t *anchor, int32_t B,
+                                       const int32_t *target, int32_t *path, int32_t *accept_len, int32_t *emitted,
+                                       int32_t *topk_ids, float *topk_vals, float *pair_scores, float *path_score,
+                                       uint8_t *tie_flags, void *stream)
+{
+    if (h && h->cfg.walk == DFLASH_WALK_SAMPLE)
+        return fail(DFLASH_ERR_INVALID_ARG, "a sampling handle runs through dflash_select_run_sampled");
+    if (B > 0 && (!target || !accept_len)) return fail(DFLASH_ERR_INVALID_ARG, "target and accept_len must not be NULL");
+    return run_impl(h, hidden, anchor, B, nullptr, topk_ids, topk_vals, pair_scores, path, nullptr, path_score,
+                    tie_flags, stream, target, accept_len, emitted);
 }
 
 dflash_status dflash_select_run_sampled(dflash_select_handle h, const void *hidden, const int32_t *anchor,
@@ -936,10 +957,9 @@ dflash_status dflash_select_step_host(dflash_select_handle h, const void *hidden
     CUDA_TRY(cudaMemcpyAsync(c->st_hidden, hidden_host, nb * L * c->cfg.d * 2, cudaMemcpyHostToDevice, s));
     CUDA_TRY(cudaMemcpyAsync(c->st_anchor, anchor_host, nb * 4, cudaMemcpyHostToDevice, s));
     CUDA_TRY(cudaMemcpyAsync(c->st_target, target_host, nb * (L + 1) * 4, cudaMemcpyHostToDevice, s));
-    dflash_status st = dflash_select_run(h, c->st_hidden, c->st_anchor, B, nullptr, nullptr, nullptr, c->st_path,
-                                         nullptr, nullptr, stream);
-    if (st != DFLASH_OK) return st;
-    st = dflash_verify_prefix(c->st_path, c->st_target, B, L, c->st_accept, c->st_emitted, stream);
+    dflash_status st = dflash_select_run_verify(h, c->st_hidden, c->st_anchor, B, c->st_target, c->st_path,
+                                                c->st_accept, c->st_emitted, nullptr, nullptr, nullptr, nullptr,
+                                                nullptr, stream);
     if (st != DFLASH_OK) return st;
     CUDA_TRY(cudaMemcpyAsync(path_host, c->st_path, nb * L * 4, cudaMemcpyDeviceToHost, s));
     CUDA_TRY(cudaMemcpyAsync(accept_host, c->st_accept, nb * 4, cudaMemcpyDeviceToHost, s));

@@ -185,6 +185,9 @@ struct PairParams {
     float temperature;
     const uint64_t *dd_tab = nullptr;  // deduplicated AB rows: the row of token v is
     const int32_t *dd_rep = nullptr;   // dd_rep[~low32(dd_tab[v])] (NULL: AB by gathered row)
+    const int32_t *target = nullptr;   // [B, L+1] target tokens: the walker also checks the path (NULL: not)
+    int32_t *accept = nullptr;         // [B]
+    int32_t *emitted = nullptr;        // [B, L+1] (may be NULL)
 };
 cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s);
 
@@ -214,6 +217,9 @@ struct TailParams {
     const float *u_walk;  // [B, L] uniforms (sampling walk)
     float *q_out;         // [B, L, K] draft distributions (sampling walk)
     float temperature;
+    const int32_t *target = nullptr;  // [B, L+1] target tokens: the walker also checks the path (NULL: not)
+    int32_t *accept = nullptr;        // [B]
+    int32_t *emitted = nullptr;       // [B, L+1] (may be NULL)
 };
 int tail_cluster_size(int d);
 int tail_stages(int K, int G, int cs, int smem_optin);

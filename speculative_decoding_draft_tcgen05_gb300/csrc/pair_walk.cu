@@ -171,7 +171,10 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
                      p.path_score ? p.path_score + b : nullptr,
                      p.tie_flags ? p.tie_flags + static_cast<size_t>(b) * L : nullptr,
                      SampleArgs{p.u_walk ? p.u_walk + static_cast<size_t>(b) * L : nullptr,
-                                p.q_out ? p.q_out + static_cast<size_t>(b) * L * K : nullptr, p.temperature});
+                                p.q_out ? p.q_out + static_cast<size_t>(b) * L * K : nullptr, p.temperature},
+                     VerifyArgs{p.target ? p.target + static_cast<size_t>(b) * (L + 1) : nullptr,
+                                p.accept ? p.accept + b : nullptr,
+                                p.emitted ? p.emitted + static_cast<size_t>(b) * (L + 1) : nullptr});
 }
 
 }  // namespace

@@ -34,6 +34,14 @@ struct SampleArgs {
     float temperature;
 };
 
+// The greedy accept check of the walked path, done by the walking warp when
+// the caller passes the target's argmax tokens (NULL target: not done).
+struct VerifyArgs {
+    const int32_t *target;  // [L + 1] target argmax tokens after x0, path[0], ...
+    int32_t *accept;        // [1] n = leading positions with path[t] == target[t]
+    int32_t *emitted;       // [L + 1] path[0..n-1], target[n], then -1 (may be NULL)
+};
+
 // Called by every thread of a 256-thread CTA, uniformly. Stages the L tables
 // P_seq [L, K, K] and the candidates ids_seq [L, K] (written by other CTAs of
 // this or an earlier kernel; read around L1) into shared memory (Pb, ws.ids),
@@ -53,7 +61,8 @@ struct SampleArgs {
 template <int K>
 __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t *ids_seq, int L, int walk,
                                               float tie_eps, float *Pb, WalkSmem<K> &ws, int32_t *path_out,
-                                              float *score_out, uint8_t *flags_out, SampleArgs sa = {})
+                                              float *score_out, uint8_t *flags_out, SampleArgs sa = {},
+                                              VerifyArgs va = {})
 {
     const int tid = threadIdx.x;
     {
@@ -214,11 +223,19 @@ __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t 
         score = total;
     }
     __syncwarp();
+    const int32_t tok = (lane < L) ? ws.ids[lane * K + ws.ranks[lane]] : 0;
     if (lane < L) {
-        path_out[lane] = ws.ids[lane * K + ws.ranks[lane]];
+        path_out[lane] = tok;
         if (flags_out) flags_out[lane] = ws.flags[lane];
     }
     if (lane == 0 && score_out) *score_out = score;
+    if (va.target) {
+        const int32_t tg = (lane <= L) ? __ldg(va.target + lane) : 0;
+        const unsigned miss = __ballot_sync(0xFFFFFFFFu, lane < L && tok != tg);
+        const int n = miss ? __ffs(miss) - 1 : L;
+        if (lane == 0) *va.accept = n;
+        if (va.emitted && lane <= L) va.emitted[lane] = (lane < n) ? tok : (lane == n ? tg : -1);
+    }
 }
 
 }  // namespace dfl

@@ -284,3 +284,36 @@ def test_init_reports_a_failed_device_allocation(pkg):
     full = parity.run_gpu(inp, dtensors=d)
     orc = parity.run_oracle(inp, range(w.B))
     assert parity.compare(inp, full, orc)["path_equal"] == w.B
+
+
+@pytest.mark.parametrize("name,seqs", [("tiny", None), ("4b_b8", None)])
+def test_run_verify_equals_run_then_verify(pkg, name, seqs):
+    """The fused run + accept check gives the outputs of dflash_select_run
+    followed by dflash_verify_prefix, on the small-batch fused tail (tiny) and on
+    the pair-table kernel (batch 8), with accept lengths spanning 0..L."""
+    inp = parity.inputs_for(name)
+    w = inp.wl
+    d = parity.to_device(inp, "cuda")
+    sel_seqs = list(range(w.B))
+    orc = parity.run_oracle(inp, sel_seqs)
+    path = torch.stack([torch.from_numpy(orc[s]["tokens"]) for s in sel_seqs])
+    n0 = torch.arange(w.B, dtype=torch.int32) % (w.L + 1)
+    tgt = wl.plant_targets(path, inp.target_rand, n0, w.V)
+    ref = parity.run_gpu(inp, dtensors=d, targets=tgt)
+    with pkg.Selector(d["W"], d["E"], d["W_A"], d["W_B"], d["W_H"], L=w.L, K=w.K, max_batch=w.B,
+                      tie_eps=parity.TIE_EPS) as sel:
+        out = sel.outputs(w.B)
+        acc = torch.full((w.B,), -5, dtype=torch.int32, device="cuda")
+        em = torch.full((w.B, w.L + 1), -5, dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            pkg.dflash_select_run_verify(sel.h, d["hidden"], d["anchor"], tgt.cuda(), accept_len=acc, emitted=em,
+                                         **out)
+            pkg.dflash_select_sync_status(sel.h)
+            got = {k: v.cpu().numpy() for k, v in out.items()}
+            for k in ("topk_ids", "topk_vals", "pair_scores", "path", "path_score", "tie_flags"):
+                assert np.array_equal(got[k], ref[k]), k
+            assert np.array_equal(acc.cpu().numpy(), ref["accept"]) and np.array_equal(em.cpu().numpy(), ref["emitted"])
+    got["accept"], got["emitted"] = acc.cpu().numpy(), em.cpu().numpy()
+    rep = parity.compare(inp, got, orc, targets={s: tgt[s].numpy() for s in sel_seqs})
+    assert rep["accept_checked"] == w.B
+    assert sorted(set(got["accept"].tolist())) == sorted(set(n0.tolist()))
