@@ -23,12 +23,24 @@ namespace {
 // grid B * L; block 256. Builds S_t for one (sequence, position); the last
 // CTA of a sequence to finish walks its tables. Every global load batch is
 // issued in full before its values are used (one round trip per batch).
+// Agt and Bt hold K values per component k in rows of K / 4 float4 units;
+// unit u of row k sits at u ^ pw_swz<K>(k), so that the float4 stores of eight
+// consecutive components (one shared-memory phase) hit eight different banks
+// groups, and a row's units stay a permutation of the row for the readers.
 template <int K>
-__global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
+__device__ __forceinline__ int pw_swz(int k)
+{
+    static_assert(K == 16 || K == 32, "K is 16 or 32");
+    constexpr int U = K / 4;
+    return (k / (8 / U)) % U;
+}
+
+template <int K>
+__global__ void __launch_bounds__(256, (K == 16) ? 4 : 2) pair_walk_kernel(const PairParams p)
 {
     extern __shared__ float pw_smem[];
-    float *const Agt = pw_smem;                // (A(prev_i) (.) g_t)[k] at [k * K + i]
-    float *const Bt = pw_smem + kEmbed * K;    // B(c_{t,j})[k] at [k * K + j]
+    float *const Agt = pw_smem;                // (A(prev_i) (.) g_t)[k], row k, swizzled units
+    float *const Bt = pw_smem + kEmbed * K;    // B(c_{t,j})[k], row k, swizzled units
     __shared__ float vals[K];
     __shared__ WalkSmem<K> ws;
     __shared__ int is_last;
@@ -95,10 +107,14 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
             for (int j = 0; j < K; ++j) bb[j] = p.AB[(rowB0 + j) * 512 + kEmbed + k];
         }
         const float v = (tid < K) ? p.vals[pos * K + tid] : 0.f;
+        float4 *const a4 = reinterpret_cast<float4 *>(Agt + k * K);
+        float4 *const b4 = reinterpret_cast<float4 *>(Bt + k * K);
+        const int sw = pw_swz<K>(k);
 #pragma unroll
-        for (int i = 0; i < K; ++i) Agt[k * K + i] = a[i] * gk;
-#pragma unroll
-        for (int j = 0; j < K; ++j) Bt[k * K + j] = bb[j];
+        for (int u = 0; u < K / 4; ++u) {
+            a4[u ^ sw] = make_float4(a[4 * u] * gk, a[4 * u + 1] * gk, a[4 * u + 2] * gk, a[4 * u + 3] * gk);
+            b4[u ^ sw] = make_float4(bb[4 * u], bb[4 * u + 1], bb[4 * u + 2], bb[4 * u + 3]);
+        }
         if (tid < K) vals[tid] = v;
     }
     __syncthreads();
@@ -120,14 +136,18 @@ __global__ void __launch_bounds__(256) pair_walk_kernel(const PairParams p)
 #pragma unroll 4
         for (int k = kg * 64; k < kg * 64 + 64; ++k) {
             float a[RT], bb[RT];
+            // the RT values at columns c .. c + RT - 1 lie in one float4 unit
+            const int sw = pw_swz<K>(k);
+            const int ca = (((bi * RT) >> 2) ^ sw) * 4 + ((bi * RT) & 3);
+            const int cb = (((bj * RT) >> 2) ^ sw) * 4 + ((bj * RT) & 3);
             if constexpr (RT == 4) {
-                const float4 av = *reinterpret_cast<const float4 *>(Agt + k * K + bi * RT);
-                const float4 bv = *reinterpret_cast<const float4 *>(Bt + k * K + bj * RT);
+                const float4 av = *reinterpret_cast<const float4 *>(Agt + k * K + ca);
+                const float4 bv = *reinterpret_cast<const float4 *>(Bt + k * K + cb);
                 a[0] = av.x, a[1] = av.y, a[2] = av.z, a[3] = av.w;
                 bb[0] = bv.x, bb[1] = bv.y, bb[2] = bv.z, bb[3] = bv.w;
             } else {
-                const float2 av = *reinterpret_cast<const float2 *>(Agt + k * K + bi * RT);
-                const float2 bv = *reinterpret_cast<const float2 *>(Bt + k * K + bj * RT);
+                const float2 av = *reinterpret_cast<const float2 *>(Agt + k * K + ca);
+                const float2 bv = *reinterpret_cast<const float2 *>(Bt + k * K + cb);
                 a[0] = av.x, a[1] = av.y;
                 bb[0] = bv.x, bb[1] = bv.y;
             }

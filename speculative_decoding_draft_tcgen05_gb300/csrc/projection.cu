@@ -277,22 +277,34 @@ __global__ void __launch_bounds__(kPrThreads, 1) projection_tc_kernel(const __gr
         }
         __syncthreads();
         if (last) {
+            // d is split in two halves (projection_ksplit); the loads of a
+            // batch of items are all issued before any sum is stored, so a
+            // batch costs one round trip to L2
             __threadfence();
             constexpr int nc4 = NC / 4;
+            constexpr int kSumBatch = 8;
             const size_t zstride = static_cast<size_t>(p.R_total) * 512;
-            for (int e = threadIdx.x; e < kPrRows * nc4; e += kPrThreads) {
-                const int gr = row0 + e / nc4;
-                if (gr >= n_rows) break;  // e grows with the row
-                const size_t off = static_cast<size_t>(gr) * 512 + ct * NC + (e % nc4) * 4;
-                float4 acc = __ldcg(reinterpret_cast<const float4 *>(p.part + off));
-                for (int z = 1; z < p.ksplit; ++z) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(p.part + z * zstride + off));
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
+            const int n_items = max(0, min(kPrRows, n_rows - row0)) * nc4;
+            for (int e0 = threadIdx.x; e0 < n_items; e0 += kSumBatch * kPrThreads) {
+                float4 h0[kSumBatch], h1[kSumBatch];
+#pragma unroll
+                for (int u = 0; u < kSumBatch; ++u) {
+                    const int e = e0 + u * kPrThreads;
+                    if (e < n_items) {
+                        const size_t off = static_cast<size_t>(row0 + e / nc4) * 512 + ct * NC + (e % nc4) * 4;
+                        h0[u] = __ldcg(reinterpret_cast<const float4 *>(p.part + off));
+                        h1[u] = __ldcg(reinterpret_cast<const float4 *>(p.part + zstride + off));
+                    }
                 }
-                *reinterpret_cast<float4 *>(p.AB + off) = acc;
+#pragma unroll
+                for (int u = 0; u < kSumBatch; ++u) {
+                    const int e = e0 + u * kPrThreads;
+                    if (e < n_items) {
+                        const size_t off = static_cast<size_t>(row0 + e / nc4) * 512 + ct * NC + (e % nc4) * 4;
+                        *reinterpret_cast<float4 *>(p.AB + off) = make_float4(h0[u].x + h1[u].x, h0[u].y + h1[u].y,
+                                                                              h0[u].z + h1[u].z, h0[u].w + h1[u].w);
+                    }
+                }
             }
         }
     }
@@ -370,6 +382,7 @@ cudaError_t launch_dedup_compact(const DedupParams &d, const int32_t *ids, int R
 
 cudaError_t launch_projection(const ProjParams &p, int NC, cudaStream_t s)
 {
+    if (p.ksplit < 1 || p.ksplit > 2) return cudaErrorInvalidValue;  // the sum adds two halves
     const dim3 grid(512 / NC, (p.R_total + kPrRows - 1) / kPrRows, p.ksplit);
     if (NC == 64) return launch_ex(projection_tc_kernel<64>, grid, dim3(kPrThreads), PrShape<64>::kSmem, s, 1, p);
     if (NC == 128) return launch_ex(projection_tc_kernel<128>, grid, dim3(kPrThreads), PrShape<128>::kSmem, s, 1, p);
