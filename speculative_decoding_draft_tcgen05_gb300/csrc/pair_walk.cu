@@ -122,10 +122,13 @@ __global__ void __launch_bounds__(256, (K == 16) ? 4 : 2) pair_walk_kernel(const
     float *Pt = p.P + pos * K * K;
     float *Po = p.P_out ? p.P_out + pos * K * K : nullptr;
     {
-        // Register tiles: thread (kg, bi, bj) sums components [64 kg, 64 kg + 64)
-        // of the RT x RT pairs (bi RT + r1, bj RT + r2), RT = K / 8, reading RT
+        // Register tiles: thread (kg, bi, bj) sums, over its component group
+        // kg, the RT x RT pairs (bi RT + r1, bj RT + r2), RT = K / 8, reading RT
         // values of each operand per component (one vector load each), so shared
         // memory serves RT^2 FMAs per two loads instead of one FMA per two.
+        // Group kg holds the components k = 8 j + 2 kg + e (j < 32, e < 2): their
+        // rows share one swizzle (K = 16: pw_swz = kg) or two (K = 32: 2 kg + e),
+        // so the column offsets of the loads do not change along the loop.
         constexpr int RT = K / 8;
         const int kg = tid >> 6, bi = (tid >> 3) & 7, bj = tid & 7;
         float acc[RT][RT];
@@ -133,28 +136,38 @@ __global__ void __launch_bounds__(256, (K == 16) ? 4 : 2) pair_walk_kernel(const
         for (int r1 = 0; r1 < RT; ++r1)
 #pragma unroll
             for (int r2 = 0; r2 < RT; ++r2) acc[r1][r2] = 0.f;
+        int ca[2], cb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int sw = (K == 16) ? kg : 2 * kg + e;  // pw_swz<K>(8 j + 2 kg + e)
+            ca[e] = (bi * RT) ^ (sw << 2);
+            cb[e] = (bj * RT) ^ (sw << 2);
+        }
+        const float *arow = Agt + (2 * kg) * K;
+        const float *brow = Bt + (2 * kg) * K;
 #pragma unroll 4
-        for (int k = kg * 64; k < kg * 64 + 64; ++k) {
-            float a[RT], bb[RT];
-            // the RT values at columns c .. c + RT - 1 lie in one float4 unit
-            const int sw = pw_swz<K>(k);
-            const int ca = (((bi * RT) >> 2) ^ sw) * 4 + ((bi * RT) & 3);
-            const int cb = (((bj * RT) >> 2) ^ sw) * 4 + ((bj * RT) & 3);
-            if constexpr (RT == 4) {
-                const float4 av = *reinterpret_cast<const float4 *>(Agt + k * K + ca);
-                const float4 bv = *reinterpret_cast<const float4 *>(Bt + k * K + cb);
-                a[0] = av.x, a[1] = av.y, a[2] = av.z, a[3] = av.w;
-                bb[0] = bv.x, bb[1] = bv.y, bb[2] = bv.z, bb[3] = bv.w;
-            } else {
-                const float2 av = *reinterpret_cast<const float2 *>(Agt + k * K + ca);
-                const float2 bv = *reinterpret_cast<const float2 *>(Bt + k * K + cb);
-                a[0] = av.x, a[1] = av.y;
-                bb[0] = bv.x, bb[1] = bv.y;
+        for (int j = 0; j < 32; ++j) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float a[RT], bb[RT];
+                if constexpr (RT == 4) {
+                    const float4 av = *reinterpret_cast<const float4 *>(arow + e * K + ca[e]);
+                    const float4 bv = *reinterpret_cast<const float4 *>(brow + e * K + cb[e]);
+                    a[0] = av.x, a[1] = av.y, a[2] = av.z, a[3] = av.w;
+                    bb[0] = bv.x, bb[1] = bv.y, bb[2] = bv.z, bb[3] = bv.w;
+                } else {
+                    const float2 av = *reinterpret_cast<const float2 *>(arow + e * K + ca[e]);
+                    const float2 bv = *reinterpret_cast<const float2 *>(brow + e * K + cb[e]);
+                    a[0] = av.x, a[1] = av.y;
+                    bb[0] = bv.x, bb[1] = bv.y;
+                }
+#pragma unroll
+                for (int r1 = 0; r1 < RT; ++r1)
+#pragma unroll
+                    for (int r2 = 0; r2 < RT; ++r2) acc[r1][r2] = fmaf(a[r1], bb[r2], acc[r1][r2]);
             }
-#pragma unroll
-            for (int r1 = 0; r1 < RT; ++r1)
-#pragma unroll
-                for (int r2 = 0; r2 < RT; ++r2) acc[r1][r2] = fmaf(a[r1], bb[r2], acc[r1][r2]);
+            arow += 8 * K;
+            brow += 8 * K;
         }
         __syncthreads();  // every thread is done with Agt / Bt
         float *const part = pw_smem;  // [4 component groups][K * K], over Agt

@@ -65,6 +65,9 @@ __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t 
                                               VerifyArgs va = {})
 {
     const int tid = threadIdx.x;
+    // the target tokens of the accept check do not depend on the walk: loaded
+    // with the tables, not after the path is known
+    const int32_t tg = (va.target && tid <= L) ? __ldg(va.target + tid) : 0;
     {
         int32_t idv[2];
 #pragma unroll
@@ -230,7 +233,6 @@ __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t 
     }
     if (lane == 0 && score_out) *score_out = score;
     if (va.target) {
-        const int32_t tg = (lane <= L) ? __ldg(va.target + lane) : 0;
         const unsigned miss = __ballot_sync(0xFFFFFFFFu, lane < L && tok != tg);
         const int n = miss ? __ffs(miss) - 1 : L;
         if (lane == 0) *va.accept = n;
