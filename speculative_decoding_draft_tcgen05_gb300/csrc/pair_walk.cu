@@ -46,7 +46,6 @@ __global__ void __launch_bounds__(256, (K == 16) ? 4 : 2) pair_walk_kernel(const
     __shared__ int is_last;
     __shared__ int32_t dd_row[2 * K];  // deduplicated AB rows of the predecessors and the candidates
 
-    pdl_trigger();
     pdl_wait();
     const int L = p.L, R = p.R;
     const int b = blockIdx.x / L, t = blockIdx.x % L;
@@ -118,6 +117,9 @@ __global__ void __launch_bounds__(256, (K == 16) ? 4 : 2) pair_walk_kernel(const
         if (tid < K) vals[tid] = v;
     }
     __syncthreads();
+    // the next kernel (the next lm_head pass) is scheduled once every CTA has
+    // its operands: its early weight loads no longer compete with these
+    pdl_trigger();
 
     float *Pt = p.P + pos * K * K;
     float *Po = p.P_out ? p.P_out + pos * K * K : nullptr;

@@ -140,7 +140,6 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
         fence_mbar_init();
     }
     __syncthreads();
-    pdl_trigger();
     const bool tab = p.tab != nullptr;  // precomputed A|B rows: no projections here
     const int pre = nkb < S ? nkb : S;
     if (tid == 0 && !tab) {
@@ -443,6 +442,11 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
         }
     }
     __syncthreads();
+    // The next kernel on the stream (the next lm_head pass) may be scheduled
+    // from here: its early weight loads would compete with this kernel's
+    // memory phases (measured: 0.85 us per batch-1 step); the other CTAs
+    // count as triggered when they exit.
+    pdl_trigger();
     if (!is_last) return;
     walk_sequence<K>(p.P + static_cast<size_t>(b) * L * K * K, p.ids + static_cast<size_t>(b) * L * K, L, p.walk,
                      p.tie_eps, reinterpret_cast<float *>(gbase), ws, p.path + static_cast<size_t>(b) * L,
