@@ -126,7 +126,7 @@ def kernel_src_digest():
             h.update(fh.read())
     with open(os.path.join(csrc, "kernels.h"), "rb") as fh:
         text = fh.read()
-    cut = text.find(b"// ---- candidate projections")
+    cut = text.find(b"// ---- candidate deduplication")
     h.update(text if cut < 0 else text[:cut])
     return h.hexdigest()
 

@@ -449,4 +449,19 @@ __device__ __forceinline__ uint64_t list_merge(uint64_t a, uint64_t b, int lane,
     return (lane < K) ? c : 0;
 }
 
+// Bitonic sort of one 32-bit value per lane, descending (lane 0 largest).
+__device__ __forceinline__ uint32_t warp_sort_desc_u32(uint32_t x, int lane)
+{
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int jm = k >> 1; jm > 0; jm >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, x, jm);
+            const bool keep_max = ((lane & jm) == 0) == ((lane & k) == 0);
+            x = keep_max ? (x > o ? x : o) : (x < o ? x : o);
+        }
+    }
+    return x;
+}
+
 }  // namespace dfl

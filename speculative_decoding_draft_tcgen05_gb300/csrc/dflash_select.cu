@@ -379,6 +379,7 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
                     prop.minor);
 
     CUDA_TRY(dfl::prepare_lmhead(static_cast<int>(prop.sharedMemPerBlockOptin)));
+    CUDA_TRY(dfl::prepare_topk_merge(static_cast<int>(prop.sharedMemPerBlockOptin)));
     CUDA_TRY(dfl::prepare_pair_walk(static_cast<int>(prop.sharedMemPerBlockOptin)));
     CUDA_TRY(dfl::prepare_projection(static_cast<int>(prop.sharedMemPerBlockOptin)));
     CUDA_TRY(dfl::prepare_tail(static_cast<int>(prop.sharedMemPerBlockOptin)));

@@ -59,6 +59,7 @@ cudaError_t set_max_dynamic_smem(void (*kern)(KArgs...), int smem_optin)
 // Sets the shared-memory opt-ins of every kernel on the current device
 // (smem_optin = cudaDevAttrMaxSharedMemoryPerBlockOptin).
 cudaError_t prepare_lmhead(int smem_optin);
+cudaError_t prepare_topk_merge(int smem_optin);
 cudaError_t prepare_pair_walk(int smem_optin);
 
 // ---- lm_head GEMM + streaming top-K (and the context gate g = W_H h) ----

@@ -81,7 +81,7 @@ dflash_status setup_current_device(DeviceSetup *out)
         cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess || !ptr)
             return fail(DFLASH_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed (error %lld)", e);
-        if (dfl::prepare_lmhead(optin) != cudaSuccess)
+        if (dfl::prepare_lmhead(optin) != cudaSuccess || dfl::prepare_topk_merge(optin) != cudaSuccess)
             return fail(DFLASH_ERR_CUDA, "setting the kernels' shared-memory limit failed");
         s.num_sms = sms;
         s.smem_optin = optin;
