@@ -278,6 +278,28 @@ def dflash_select_step_host(handle, hidden_host, anchor_host, target_host, path_
                                          _stream(stream)), "dflash_select_step_host")
 
 
+def bind_step_host(handle, hidden_host, anchor_host, target_host, path_host, accept_host, emitted_host,
+                   stream=None):
+    """Marshals the arguments of dflash_select_step_host once and returns a
+    zero-argument callable that makes the same call again; for tight loops
+    over fixed host buffers."""
+    import torch
+    B = anchor_host.shape[0]
+    args = (handle, _ptr(hidden_host, torch.bfloat16, "hidden_host", device=False),
+            _ptr(anchor_host, torch.int32, "anchor_host", device=False),
+            _ptr(target_host, torch.int32, "target_host", device=False), B,
+            _ptr(path_host, torch.int32, "path_host", device=False),
+            _ptr(accept_host, torch.int32, "accept_host", device=False),
+            _ptr(emitted_host, torch.int32, "emitted_host", device=False), _stream(stream))
+    fn = lib().dflash_select_step_host
+
+    def step():
+        st = fn(*args)
+        if st:
+            _check(st, "dflash_select_step_host")
+    return step
+
+
 def dflash_select_sync_status(handle, stream=None) -> int:
     """Waits for the stream; returns the latched device status (raises on error)."""
     st = lib().dflash_select_sync_status(handle, _stream(stream))

@@ -185,10 +185,14 @@ struct dflash_select_ctx {
     int32_t *dd_uniq = nullptr, *dd_rep = nullptr;  // [max_batch * R]
     uint32_t dd_epoch = 0;
     int *err = nullptr;
-    // staging of dflash_select_step_host
+    // staging of dflash_select_step_host: on the device [anchor | target] (one
+    // upload) and [error word | path | accept | emitted] (one read-back), with
+    // pinned host images of both at the same offsets
     uint16_t *st_hidden = nullptr;
     int32_t *st_anchor = nullptr, *st_target = nullptr, *st_path = nullptr, *st_accept = nullptr,
             *st_emitted = nullptr;
+    size_t st_in_bytes = 0, st_out_bytes = 0;  // spans of the two blocks
+    uint8_t *st_in_host = nullptr, *st_out_host = nullptr;  // pinned
     int *err_host = nullptr;  // pinned
 
     bool prof = false;
@@ -454,24 +458,31 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     const size_t o_ddcnt = off; off += up(cfg->dedup ? 4 : 0);
     const size_t o_dduniq = off; off += up(dd_rows * 4);
     const size_t o_ddrep = off; off += up(dd_rows * 4);
-    const size_t o_err = off; off += up(4);
     const size_t o_hid = off; off += up(Nmax * cfg->d * 2);
     const size_t o_anc = off; off += up(Bm * 4);
     const size_t o_tgt = off; off += up(Bm * (cfg->L + 1) * 4);
+    const size_t o_err = off; off += up(4);  // the error word leads the read-back block
     const size_t o_path = off; off += up(Nmax * 4);
     const size_t o_acc = off; off += up(Bm * 4);
     const size_t o_emit = off; off += up(Bm * (cfg->L + 1) * 4);
+    const size_t in_bytes = o_err - o_anc, out_bytes = off - o_err;
     cudaError_t e = cudaMalloc(&c->ws, off);
     if (e != cudaSuccess) {
         delete c;
         return fail(DFLASH_ERR_CUDA, "cudaMalloc of a %zu-byte workspace failed: %s", off, cudaGetErrorString(e));
     }
-    e = cudaMallocHost(&c->err_host, sizeof(int));
+    // one pinned allocation: the error word, then the images of the two staging blocks
+    const size_t host_bytes = up(sizeof(int)) + up(in_bytes) + out_bytes;
+    e = cudaMallocHost(&c->err_host, host_bytes);
     if (e != cudaSuccess) {
         cudaFree(c->ws);
         delete c;
-        return fail(DFLASH_ERR_CUDA, "cudaMallocHost failed: %s", cudaGetErrorString(e));
+        return fail(DFLASH_ERR_CUDA, "cudaMallocHost of %zu bytes failed: %s", host_bytes, cudaGetErrorString(e));
     }
+    c->st_in_host = reinterpret_cast<uint8_t *>(c->err_host) + up(sizeof(int));
+    c->st_out_host = c->st_in_host + up(in_bytes);
+    c->st_in_bytes = in_bytes;
+    c->st_out_bytes = out_bytes;
     uint8_t *w = static_cast<uint8_t *>(c->ws);
     c->part = reinterpret_cast<uint64_t *>(w + o_part);
     c->thr_g = reinterpret_cast<uint64_t *>(w + o_thrg);
@@ -955,17 +966,39 @@ dflash_status dflash_select_step_host(dflash_select_handle h, const void *hidden
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int L = c->cfg.L;
     const size_t nb = static_cast<size_t>(B);
+    // the previous call ended with a synchronisation, so the pinned images are free
+    uint8_t *const in_host = c->st_in_host;
+    const size_t tgt_off = reinterpret_cast<uint8_t *>(c->st_target) - reinterpret_cast<uint8_t *>(c->st_anchor);
+    std::memcpy(in_host, anchor_host, nb * 4);
+    std::memcpy(in_host + tgt_off, target_host, nb * (L + 1) * 4);
     CUDA_TRY(cudaMemcpyAsync(c->st_hidden, hidden_host, nb * L * c->cfg.d * 2, cudaMemcpyHostToDevice, s));
-    CUDA_TRY(cudaMemcpyAsync(c->st_anchor, anchor_host, nb * 4, cudaMemcpyHostToDevice, s));
-    CUDA_TRY(cudaMemcpyAsync(c->st_target, target_host, nb * (L + 1) * 4, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(c->st_anchor, in_host, tgt_off + nb * (L + 1) * 4, cudaMemcpyHostToDevice, s));
     dflash_status st = dflash_select_run_verify(h, c->st_hidden, c->st_anchor, B, c->st_target, c->st_path,
                                                 c->st_accept, c->st_emitted, nullptr, nullptr, nullptr, nullptr,
                                                 nullptr, stream);
     if (st != DFLASH_OK) return st;
-    CUDA_TRY(cudaMemcpyAsync(path_host, c->st_path, nb * L * 4, cudaMemcpyDeviceToHost, s));
-    CUDA_TRY(cudaMemcpyAsync(accept_host, c->st_accept, nb * 4, cudaMemcpyDeviceToHost, s));
-    CUDA_TRY(cudaMemcpyAsync(emitted_host, c->st_emitted, nb * (L + 1) * 4, cudaMemcpyDeviceToHost, s));
-    return read_device_error(c, s);
+    // one read-back of the error word and the results, then one synchronisation
+    uint8_t *const out_dev = reinterpret_cast<uint8_t *>(c->err);
+    const size_t emit_end =
+        static_cast<size_t>(reinterpret_cast<uint8_t *>(c->st_emitted) - out_dev) + nb * (L + 1) * 4;
+    CUDA_TRY(cudaMemcpyAsync(c->st_out_host, out_dev, emit_end, cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    int e;
+    std::memcpy(&e, c->st_out_host, sizeof(int));
+    if (e != 0) {
+        CUDA_TRY(cudaMemsetAsync(c->err, 0, sizeof(int), s));
+        CUDA_TRY(cudaStreamSynchronize(s));
+        if (e & dfl::DEV_ERR_TIMEOUT)
+            return fail(DFLASH_ERR_TIMEOUT, "a kernel pipeline wait exceeded its time bound (device error word %d)",
+                        e);
+        return fail(DFLASH_ERR_DEVICE_CHECK, "a token id outside [0, V) reached the selector (device error word %d)",
+                    e);
+    }
+    auto host_at = [&](const int32_t *dev) { return c->st_out_host + (reinterpret_cast<const uint8_t *>(dev) - out_dev); };
+    std::memcpy(path_host, host_at(c->st_path), nb * L * 4);
+    std::memcpy(accept_host, host_at(c->st_accept), nb * 4);
+    std::memcpy(emitted_host, host_at(c->st_emitted), nb * (L + 1) * 4);
+    return ok();
 }
 
 dflash_status dflash_select_sync_status(dflash_select_handle h, void *stream)

@@ -200,6 +200,42 @@ def test_step_from_host_buffers(pkg):
                 assert path[b].tolist() == orc[b]["tokens"].tolist() and em[b].tolist() == e.tolist()
 
 
+def test_step_host_bound_pageable_and_error(pkg):
+    """The pre-bound host step equals the plain call, pageable host buffers
+    work too, and a latched device error comes back through the one read-back
+    (then the handle runs cleanly again)."""
+    inp = parity.inputs_for("tiny")
+    d = parity.to_device(inp, "cuda")
+    w = inp.wl
+    full = parity.run_gpu(inp, dtensors=d)
+    tgt = wl.plant_targets(torch.from_numpy(full["path"]), inp.target_rand, torch.tensor([2, 7], dtype=torch.int32),
+                           w.V)
+    with pkg.Selector(d["W"], d["E"], d["W_A"], d["W_B"], d["W_H"], L=w.L, K=w.K, max_batch=w.B) as sel:
+        outs = []
+        for pinned in (True, False):
+            mk = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+            hid, anc, tg = mk(inp.hidden), mk(inp.anchor), mk(tgt)
+            path = mk(torch.full((w.B, w.L), -5, dtype=torch.int32))
+            acc = mk(torch.full((w.B,), -5, dtype=torch.int32))
+            em = mk(torch.full((w.B, w.L + 1), -5, dtype=torch.int32))
+            step = pkg.bind_step_host(sel.h, hid, anc, tg, path, acc, em)
+            step()
+            outs.append((path.clone(), acc.clone(), em.clone()))
+            assert path.numpy().tolist() == full["path"].tolist()
+            assert acc.tolist() == [2, 7]
+        assert all(torch.equal(a, b) for a, b in zip(outs[0], outs[1]))
+        bad = inp.anchor.clone()
+        bad[1] = w.V
+        path = torch.empty(w.B, w.L, dtype=torch.int32)
+        acc = torch.empty(w.B, dtype=torch.int32)
+        em = torch.empty(w.B, w.L + 1, dtype=torch.int32)
+        with pytest.raises(pkg.DflashError) as e:
+            pkg.dflash_select_step_host(sel.h, inp.hidden, bad, tgt, path, acc, em)
+        assert e.value.status == pkg.DFLASH_ERR_DEVICE_CHECK
+        pkg.dflash_select_step_host(sel.h, inp.hidden, inp.anchor, tgt, path, acc, em)
+        assert path.numpy().tolist() == full["path"].tolist()
+
+
 def test_profile_records_kernels(pkg):
     inp = parity.inputs_for("tiny")
     d = parity.to_device(inp, "cuda")
