@@ -202,18 +202,31 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
         }
     }
     cluster.sync();
-    if (warp < nq) {
-        uint64_t x[8];
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq)
-            x[qq] = (qq < cs && lane < K) ? cluster.map_shared_rank(cta_list, qq)[warp * 32 + lane] : 0ull;
+    {
+        // the cluster's CS lists of position t - q, folded in a tree: warp
+        // 4q + w merges the lists of ranks 2w and 2w + 1, then pairs of those
+        // results, then the last two (three merges deep instead of eight)
+        const int q = warp >> 2, w4 = warp & 3;
         uint64_t r = 0;
-#pragma unroll
-        for (int qq = 0; qq < 8; ++qq)
-            if (qq < cs) r = list_merge(r, x[qq], lane, K);
-        if (lane < K) {
-            cand[warp][lane] = key_id(r);
-            if (warp == 0) cand_val[lane] = key_val(r);
+        if (q < nq) {
+            const uint64_t x0 = (2 * w4 < cs && lane < K) ? cluster.map_shared_rank(cta_list, 2 * w4)[q * 32 + lane] : 0ull;
+            const uint64_t x1 =
+                (2 * w4 + 1 < cs && lane < K) ? cluster.map_shared_rank(cta_list, 2 * w4 + 1)[q * 32 + lane] : 0ull;
+            r = list_merge(x0, x1, lane, K);
+        }
+        wl[warp][lane] = r;
+        __syncthreads();
+        if (q < nq && (w4 & 1) == 0) {
+            r = list_merge(r, wl[warp + 1][lane], lane, K);
+            wl[warp][lane] = r;
+        }
+        __syncthreads();
+        if (q < nq && w4 == 0) {
+            r = list_merge(r, wl[warp + 2][lane], lane, K);
+            if (lane < K) {
+                cand[q][lane] = key_id(r);
+                if (q == 0) cand_val[lane] = key_val(r);
+            }
         }
     }
     if (t == 0 && warp == 1 && lane < K) {
