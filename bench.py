@@ -462,7 +462,9 @@ def run_ours(args):
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world)
     h2d = hid_h.numel() * 2 + anc_h.numel() * 4 + tgt_h.numel() * 4
-    d2h = path_h.numel() * 4 + acc_h.numel() * 4 + em_h.numel() * 4 + 4
+    # path, accept, emitted, and per sequence a copy of the error word and a completion flag,
+    # written by the walking kernel into the handle's mapped pinned block
+    d2h = path_h.numel() * 4 + acc_h.numel() * 4 + em_h.numel() * 4 + 8 * w.B
 
     # the step is one dflash_select_run_verify call: the accept check runs in the walking kernel
     launches_per_step = pkg.dflash_select_launches_per_run(sel.h, w.B)
@@ -510,7 +512,7 @@ def run_ours(args):
             "clocks": clk,
             "e2e": {"value": whole_job_value(w.B, world, args.e2e_steps, e2e_s * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-                    "api": "dflash_select_step_host (pinned host buffers, copies and sync inside)"},
+                    "api": "dflash_select_step_host (pinned host buffers; two uploads; the walking kernel writes the results into mapped pinned memory, which the call polls)"},
             "gpu_launches": launches_per_step * args.steps,
         }
         if not args.no_cpu_baseline and world == 1:

@@ -179,12 +179,17 @@ dflash_status dflash_select_run_verify(dflash_select_handle h, const void *hidde
                                        uint8_t *tie_flags, void *stream);
 
 /* One whole draft-verify step from HOST buffers: copies hidden/anchor/target
- * to the handle's device staging area, runs dflash_select_run_verify, copies
- * path, accept_len and emitted back, and waits for the stream. Two uploads
- * (hidden; anchor and target through a pinned image in the handle) and one
- * read-back (the device error word and the results together, then copied to
- * the caller's buffers). hidden_host should be pinned for an asynchronous
- * copy. One call at a time per handle (the staging areas are the handle's).
+ * to the handle's device staging area (two uploads: hidden; anchor and target
+ * through a pinned image in the handle), runs dflash_select_run_verify with
+ * its results written by the walking kernel straight into a mapped pinned
+ * block of the handle, together with a copy of the device error word and a
+ * completion flag per sequence, waits for those flags (polling; after 3 s it
+ * synchronises the stream instead), and copies path, accept_len and emitted to
+ * the caller's buffers. It returns once the results are on the host: the
+ * stream may still be retiring the step's last kernel, and later work on the
+ * stream stays ordered after it. hidden_host should be pinned for an
+ * asynchronous copy. One call at a time per handle (the staging areas are the
+ * handle's).
  *   hidden_host [B, L, d] bf16, anchor_host [B], target_host [B, L+1] int32
  *   path_host [B, L], accept_host [B], emitted_host [B, L+1] int32 (outputs)
  * Returns the same errors as the two calls, and any latched device error. */

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <chrono>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -185,14 +186,23 @@ struct dflash_select_ctx {
     int32_t *dd_uniq = nullptr, *dd_rep = nullptr;  // [max_batch * R]
     uint32_t dd_epoch = 0;
     int *err = nullptr;
-    // staging of dflash_select_step_host: on the device [anchor | target] (one
-    // upload) and [error word | path | accept | emitted] (one read-back), with
-    // pinned host images of both at the same offsets
+    // staging of dflash_select_step_host: hidden and [anchor | target] on the
+    // device (two uploads, the second from a pinned image at the same
+    // offsets); the results in a mapped pinned block that the walking kernel
+    // writes directly: path [Nmax], accept [Bm], emitted [Bm, L+1], then per
+    // sequence a copy of the error word and a completion flag
     uint16_t *st_hidden = nullptr;
-    int32_t *st_anchor = nullptr, *st_target = nullptr, *st_path = nullptr, *st_accept = nullptr,
-            *st_emitted = nullptr;
-    size_t st_in_bytes = 0, st_out_bytes = 0;  // spans of the two blocks
-    uint8_t *st_in_host = nullptr, *st_out_host = nullptr;  // pinned
+    int32_t *st_anchor = nullptr, *st_target = nullptr;
+    uint8_t *st_in_host = nullptr;  // pinned image of [anchor | target]
+    int32_t *ho_path = nullptr, *ho_accept = nullptr, *ho_emitted = nullptr, *ho_err = nullptr;  // mapped, host view
+    uint32_t *ho_done = nullptr;
+    int32_t *hd_path = nullptr, *hd_accept = nullptr, *hd_emitted = nullptr, *hd_err = nullptr;  // device view
+    uint32_t *hd_done = nullptr;
+    uint32_t host_step = 0;  // the step number the flags of the latest host step carry
+    // set by dflash_select_step_host for the duration of its run
+    uint32_t *hs_done = nullptr;
+    int *hs_err_snap = nullptr;
+    uint32_t hs_step = 0;
     int *err_host = nullptr;  // pinned
 
     bool prof = false;
@@ -461,28 +471,44 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     const size_t o_hid = off; off += up(Nmax * cfg->d * 2);
     const size_t o_anc = off; off += up(Bm * 4);
     const size_t o_tgt = off; off += up(Bm * (cfg->L + 1) * 4);
-    const size_t o_err = off; off += up(4);  // the error word leads the read-back block
-    const size_t o_path = off; off += up(Nmax * 4);
-    const size_t o_acc = off; off += up(Bm * 4);
-    const size_t o_emit = off; off += up(Bm * (cfg->L + 1) * 4);
-    const size_t in_bytes = o_err - o_anc, out_bytes = off - o_err;
+    const size_t in_bytes = off - o_anc;
+    const size_t o_err = off; off += up(4);
     cudaError_t e = cudaMalloc(&c->ws, off);
     if (e != cudaSuccess) {
         delete c;
         return fail(DFLASH_ERR_CUDA, "cudaMalloc of a %zu-byte workspace failed: %s", off, cudaGetErrorString(e));
     }
-    // one pinned allocation: the error word, then the images of the two staging blocks
-    const size_t host_bytes = up(sizeof(int)) + up(in_bytes) + out_bytes;
-    e = cudaMallocHost(&c->err_host, host_bytes);
+    // one mapped pinned allocation: the error word, the image of [anchor |
+    // target], and the results block of the host step
+    const size_t h_path = up(sizeof(int)) + up(in_bytes);
+    const size_t h_acc = h_path + up(Nmax * 4);
+    const size_t h_emit = h_acc + up(Bm * 4);
+    const size_t h_err = h_emit + up(Bm * (cfg->L + 1) * 4);
+    const size_t h_done = h_err + up(Bm * 4);
+    const size_t host_bytes = h_done + up(Bm * 4);
+    e = cudaHostAlloc(&c->err_host, host_bytes, cudaHostAllocMapped);
+    uint8_t *hdev = nullptr;
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void **>(&hdev), c->err_host, 0);
     if (e != cudaSuccess) {
+        if (c->err_host) cudaFreeHost(c->err_host);
         cudaFree(c->ws);
         delete c;
-        return fail(DFLASH_ERR_CUDA, "cudaMallocHost of %zu bytes failed: %s", host_bytes, cudaGetErrorString(e));
+        return fail(DFLASH_ERR_CUDA, "mapped host allocation of %zu bytes failed: %s", host_bytes,
+                    cudaGetErrorString(e));
     }
-    c->st_in_host = reinterpret_cast<uint8_t *>(c->err_host) + up(sizeof(int));
-    c->st_out_host = c->st_in_host + up(in_bytes);
-    c->st_in_bytes = in_bytes;
-    c->st_out_bytes = out_bytes;
+    std::memset(c->err_host, 0, host_bytes);
+    uint8_t *const hhost = reinterpret_cast<uint8_t *>(c->err_host);
+    c->st_in_host = hhost + up(sizeof(int));
+    c->ho_path = reinterpret_cast<int32_t *>(hhost + h_path);
+    c->ho_accept = reinterpret_cast<int32_t *>(hhost + h_acc);
+    c->ho_emitted = reinterpret_cast<int32_t *>(hhost + h_emit);
+    c->ho_err = reinterpret_cast<int32_t *>(hhost + h_err);
+    c->ho_done = reinterpret_cast<uint32_t *>(hhost + h_done);
+    c->hd_path = reinterpret_cast<int32_t *>(hdev + h_path);
+    c->hd_accept = reinterpret_cast<int32_t *>(hdev + h_acc);
+    c->hd_emitted = reinterpret_cast<int32_t *>(hdev + h_emit);
+    c->hd_err = reinterpret_cast<int32_t *>(hdev + h_err);
+    c->hd_done = reinterpret_cast<uint32_t *>(hdev + h_done);
     uint8_t *w = static_cast<uint8_t *>(c->ws);
     c->part = reinterpret_cast<uint64_t *>(w + o_part);
     c->thr_g = reinterpret_cast<uint64_t *>(w + o_thrg);
@@ -506,9 +532,6 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     c->st_hidden = reinterpret_cast<uint16_t *>(w + o_hid);
     c->st_anchor = reinterpret_cast<int32_t *>(w + o_anc);
     c->st_target = reinterpret_cast<int32_t *>(w + o_tgt);
-    c->st_path = reinterpret_cast<int32_t *>(w + o_path);
-    c->st_accept = reinterpret_cast<int32_t *>(w + o_acc);
-    c->st_emitted = reinterpret_cast<int32_t *>(w + o_emit);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     e = cudaMemsetAsync(c->ws, 0, off, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -705,6 +728,9 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
         tp.target = target;
         tp.accept = accept;
         tp.emitted = emitted;
+        tp.done = c->hs_done;
+        tp.err_snap = c->hs_err_snap;
+        tp.step = c->hs_step;
         prof_begin(c, 1, s);
         CUDA_TRY(dfl::launch_select_tail(tp, c->cfg.K, tail_S, tail_smem, s));
         prof_end(c, 1, 4, s);
@@ -798,6 +824,9 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
     q.target = target;
     q.accept = accept;
     q.emitted = emitted;
+    q.done = c->hs_done;
+    q.err_snap = c->hs_err_snap;
+    q.step = c->hs_step;
     prof_begin(c, slot, s);
     CUDA_TRY(dfl::launch_pair_walk(q, s));
     prof_end(c, slot, 3, s);
@@ -939,6 +968,10 @@ dflash_status dflash_verify_prefix(const int32_t *path, const int32_t *target, i
     return ok();
 }
 
+// How long dflash_select_step_host polls its completion flags before it
+// synchronises the stream instead (the kernels' own waits give up after 1 s).
+constexpr int kHostWaitMs = 3000;
+
 static dflash_status read_device_error(dflash_select_ctx *c, cudaStream_t s)
 {
     CUDA_TRY(cudaMemcpyAsync(c->err_host, c->err, sizeof(int), cudaMemcpyDeviceToHost, s));
@@ -966,38 +999,55 @@ dflash_status dflash_select_step_host(dflash_select_handle h, const void *hidden
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int L = c->cfg.L;
     const size_t nb = static_cast<size_t>(B);
-    // the previous call ended with a synchronisation, so the pinned images are free
+    // the previous call returned once its walkers had finished, after the
+    // step's uploads: the pinned image is free
     uint8_t *const in_host = c->st_in_host;
     const size_t tgt_off = reinterpret_cast<uint8_t *>(c->st_target) - reinterpret_cast<uint8_t *>(c->st_anchor);
     std::memcpy(in_host, anchor_host, nb * 4);
     std::memcpy(in_host + tgt_off, target_host, nb * (L + 1) * 4);
     CUDA_TRY(cudaMemcpyAsync(c->st_hidden, hidden_host, nb * L * c->cfg.d * 2, cudaMemcpyHostToDevice, s));
     CUDA_TRY(cudaMemcpyAsync(c->st_anchor, in_host, tgt_off + nb * (L + 1) * 4, cudaMemcpyHostToDevice, s));
-    dflash_status st = dflash_select_run_verify(h, c->st_hidden, c->st_anchor, B, c->st_target, c->st_path,
-                                                c->st_accept, c->st_emitted, nullptr, nullptr, nullptr, nullptr,
+    // the walkers write the results, a copy of the error word and a flag per
+    // sequence straight into the mapped block
+    const uint32_t step = ++c->host_step;
+    c->hs_done = c->hd_done;
+    c->hs_err_snap = c->hd_err;
+    c->hs_step = step;
+    dflash_status st = dflash_select_run_verify(h, c->st_hidden, c->st_anchor, B, c->st_target, c->hd_path,
+                                                c->hd_accept, c->hd_emitted, nullptr, nullptr, nullptr, nullptr,
                                                 nullptr, stream);
+    c->hs_done = nullptr;
+    c->hs_err_snap = nullptr;
     if (st != DFLASH_OK) return st;
-    // one read-back of the error word and the results, then one synchronisation
-    uint8_t *const out_dev = reinterpret_cast<uint8_t *>(c->err);
-    const size_t emit_end =
-        static_cast<size_t>(reinterpret_cast<uint8_t *>(c->st_emitted) - out_dev) + nb * (L + 1) * 4;
-    CUDA_TRY(cudaMemcpyAsync(c->st_out_host, out_dev, emit_end, cudaMemcpyDeviceToHost, s));
-    CUDA_TRY(cudaStreamSynchronize(s));
-    int e;
-    std::memcpy(&e, c->st_out_host, sizeof(int));
-    if (e != 0) {
-        CUDA_TRY(cudaMemsetAsync(c->err, 0, sizeof(int), s));
-        CUDA_TRY(cudaStreamSynchronize(s));
-        if (e & dfl::DEV_ERR_TIMEOUT)
-            return fail(DFLASH_ERR_TIMEOUT, "a kernel pipeline wait exceeded its time bound (device error word %d)",
-                        e);
-        return fail(DFLASH_ERR_DEVICE_CHECK, "a token id outside [0, V) reached the selector (device error word %d)",
-                    e);
+    // Wait for every sequence's flag (bounded; past the bound the stream is
+    // synchronised and the device error word decides), then read the results.
+    const auto t0 = std::chrono::steady_clock::now();
+    bool all = false;
+    for (uint32_t it = 0; !all; ++it) {
+        all = true;
+        for (int32_t b = 0; b < B && all; ++b)
+            all = __atomic_load_n(c->ho_done + b, __ATOMIC_ACQUIRE) == step;
+        if (!all && (it & 1023u) == 1023u &&
+            std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(kHostWaitMs))
+            break;
     }
-    auto host_at = [&](const int32_t *dev) { return c->st_out_host + (reinterpret_cast<const uint8_t *>(dev) - out_dev); };
-    std::memcpy(path_host, host_at(c->st_path), nb * L * 4);
-    std::memcpy(accept_host, host_at(c->st_accept), nb * 4);
-    std::memcpy(emitted_host, host_at(c->st_emitted), nb * (L + 1) * 4);
+    if (!all) {
+        CUDA_TRY(cudaStreamSynchronize(s));
+        st = read_device_error(c, s);
+        if (st != DFLASH_OK) return st;
+        for (int32_t b = 0; b < B; ++b)
+            if (__atomic_load_n(c->ho_done + b, __ATOMIC_ACQUIRE) != step)
+                return fail(DFLASH_ERR_CUDA, "sequence %d of the host step produced no results", b);
+    }
+    int e = 0;
+    for (int32_t b = 0; b < B; ++b) e |= c->ho_err[b];
+    if (e != 0) {
+        CUDA_TRY(cudaStreamSynchronize(s));
+        return read_device_error(c, s);  // reports and clears the latched word
+    }
+    std::memcpy(path_host, c->ho_path, nb * L * 4);
+    std::memcpy(accept_host, c->ho_accept, nb * 4);
+    std::memcpy(emitted_host, c->ho_emitted, nb * (L + 1) * 4);
     return ok();
 }
 

@@ -189,6 +189,9 @@ struct PairParams {
     const int32_t *target = nullptr;   // [B, L+1] target tokens: the walker also checks the path (NULL: not)
     int32_t *accept = nullptr;         // [B]
     int32_t *emitted = nullptr;        // [B, L+1] (may be NULL)
+    uint32_t *done = nullptr;          // [B] host-mapped completion flags (NULL: none), set to `step`
+    int *err_snap = nullptr;           // [B] host-mapped copies of the error word
+    uint32_t step = 0;
 };
 cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s);
 
@@ -221,6 +224,9 @@ struct TailParams {
     const int32_t *target = nullptr;  // [B, L+1] target tokens: the walker also checks the path (NULL: not)
     int32_t *accept = nullptr;        // [B]
     int32_t *emitted = nullptr;       // [B, L+1] (may be NULL)
+    uint32_t *done = nullptr;         // [B] host-mapped completion flags (NULL: none), set to `step`
+    int *err_snap = nullptr;          // [B] host-mapped copies of the error word
+    uint32_t step = 0;
 };
 int tail_cluster_size(int d);
 int tail_stages(int K, int G, int cs, int smem_optin);

@@ -209,7 +209,9 @@ __global__ void __launch_bounds__(256, (K == 16) ? 4 : 2) pair_walk_kernel(const
                                 p.q_out ? p.q_out + static_cast<size_t>(b) * L * K : nullptr, p.temperature},
                      VerifyArgs{p.target ? p.target + static_cast<size_t>(b) * (L + 1) : nullptr,
                                 p.accept ? p.accept + b : nullptr,
-                                p.emitted ? p.emitted + static_cast<size_t>(b) * (L + 1) : nullptr});
+                                p.emitted ? p.emitted + static_cast<size_t>(b) * (L + 1) : nullptr,
+                                p.done ? p.done + b : nullptr, p.err_snap ? p.err_snap + b : nullptr, p.err,
+                                p.step});
 }
 
 }  // namespace

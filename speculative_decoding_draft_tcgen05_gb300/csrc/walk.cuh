@@ -40,6 +40,14 @@ struct VerifyArgs {
     const int32_t *target;  // [L + 1] target argmax tokens after x0, path[0], ...
     int32_t *accept;        // [1] n = leading positions with path[t] == target[t]
     int32_t *emitted;       // [L + 1] path[0..n-1], target[n], then -1 (may be NULL)
+    // Results written straight to mapped host memory (may be NULL): once this
+    // sequence's outputs are written, the device error word as the walker saw
+    // it goes to *err_snap and `step` to *done, each write fenced at system
+    // scope, so that a host thread polling *done can read the outputs.
+    uint32_t *done = nullptr;
+    int *err_snap = nullptr;
+    const int *err = nullptr;
+    uint32_t step = 0;
 };
 
 // Called by every thread of a 256-thread CTA, uniformly. Stages the L tables
@@ -237,6 +245,15 @@ __device__ __forceinline__ void walk_sequence(const float *P_seq, const int32_t 
         const int n = miss ? __ffs(miss) - 1 : L;
         if (lane == 0) *va.accept = n;
         if (va.emitted && lane <= L) va.emitted[lane] = (lane < n) ? tok : (lane == n ? tg : -1);
+    }
+    if (va.done) {
+        __threadfence_system();  // this lane's outputs before the flag
+        __syncwarp();
+        if (lane == 0) {
+            *va.err_snap = *reinterpret_cast<const volatile int *>(va.err);
+            __threadfence_system();
+            *reinterpret_cast<volatile uint32_t *>(va.done) = va.step;
+        }
     }
 }
 
