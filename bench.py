@@ -512,7 +512,7 @@ def run_ours(args):
             "clocks": clk,
             "e2e": {"value": whole_job_value(w.B, world, args.e2e_steps, e2e_s * 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-                    "api": "dflash_select_step_host (pinned host buffers; two uploads; the walking kernel writes the results into mapped pinned memory, which the call polls)"},
+                    "api": "dflash_select_step_host (pinned host buffers; hidden uploaded, anchor and target read by the kernels from mapped pinned memory; the walking kernel writes the results there too, and the call polls them)"},
             "gpu_launches": launches_per_step * args.steps,
         }
         if not args.no_cpu_baseline and world == 1:

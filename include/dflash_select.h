@@ -178,9 +178,10 @@ dflash_status dflash_select_run_verify(dflash_select_handle h, const void *hidde
                                        int32_t *topk_ids, float *topk_vals, float *pair_scores, float *path_score,
                                        uint8_t *tie_flags, void *stream);
 
-/* One whole draft-verify step from HOST buffers: copies hidden/anchor/target
- * to the handle's device staging area (two uploads: hidden; anchor and target
- * through a pinned image in the handle), runs dflash_select_run_verify with
+/* One whole draft-verify step from HOST buffers: copies hidden to the
+ * handle's device staging area (the one upload) and anchor/target into a
+ * mapped pinned image of the handle that the kernels read directly, runs
+ * dflash_select_run_verify with
  * its results written by the walking kernel straight into a mapped pinned
  * block of the handle, together with a copy of the device error word and a
  * completion flag per sequence, waits for those flags (polling; after 3 s it

@@ -186,14 +186,15 @@ struct dflash_select_ctx {
     int32_t *dd_uniq = nullptr, *dd_rep = nullptr;  // [max_batch * R]
     uint32_t dd_epoch = 0;
     int *err = nullptr;
-    // staging of dflash_select_step_host: hidden and [anchor | target] on the
-    // device (two uploads, the second from a pinned image at the same
-    // offsets); the results in a mapped pinned block that the walking kernel
-    // writes directly: path [Nmax], accept [Bm], emitted [Bm, L+1], then per
-    // sequence a copy of the error word and a completion flag
+    // staging of dflash_select_step_host: hidden on the device (the one
+    // upload); anchor and target in a mapped pinned image that the kernels
+    // read directly; the results in a mapped pinned block that the walking
+    // kernel writes directly: path [Nmax], accept [Bm], emitted [Bm, L+1], then
+    // per sequence a copy of the error word and a completion flag
     uint16_t *st_hidden = nullptr;
-    int32_t *st_anchor = nullptr, *st_target = nullptr;
-    uint8_t *st_in_host = nullptr;  // pinned image of [anchor | target]
+    uint8_t *st_in_host = nullptr;  // [anchor [Bm] | target [Bm, L+1] at st_tgt_off], mapped
+    uint8_t *st_in_dev = nullptr;   // its device view
+    size_t st_tgt_off = 0;
     int32_t *ho_path = nullptr, *ho_accept = nullptr, *ho_emitted = nullptr, *ho_err = nullptr;  // mapped, host view
     uint32_t *ho_done = nullptr;
     int32_t *hd_path = nullptr, *hd_accept = nullptr, *hd_emitted = nullptr, *hd_err = nullptr;  // device view
@@ -469,10 +470,8 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     const size_t o_dduniq = off; off += up(dd_rows * 4);
     const size_t o_ddrep = off; off += up(dd_rows * 4);
     const size_t o_hid = off; off += up(Nmax * cfg->d * 2);
-    const size_t o_anc = off; off += up(Bm * 4);
-    const size_t o_tgt = off; off += up(Bm * (cfg->L + 1) * 4);
-    const size_t in_bytes = off - o_anc;
     const size_t o_err = off; off += up(4);
+    const size_t tgt_off = up(Bm * 4), in_bytes = tgt_off + up(Bm * (cfg->L + 1) * 4);
     cudaError_t e = cudaMalloc(&c->ws, off);
     if (e != cudaSuccess) {
         delete c;
@@ -499,6 +498,8 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     std::memset(c->err_host, 0, host_bytes);
     uint8_t *const hhost = reinterpret_cast<uint8_t *>(c->err_host);
     c->st_in_host = hhost + up(sizeof(int));
+    c->st_in_dev = hdev + up(sizeof(int));
+    c->st_tgt_off = tgt_off;
     c->ho_path = reinterpret_cast<int32_t *>(hhost + h_path);
     c->ho_accept = reinterpret_cast<int32_t *>(hhost + h_acc);
     c->ho_emitted = reinterpret_cast<int32_t *>(hhost + h_emit);
@@ -530,8 +531,6 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     }
     c->err = reinterpret_cast<int *>(w + o_err);
     c->st_hidden = reinterpret_cast<uint16_t *>(w + o_hid);
-    c->st_anchor = reinterpret_cast<int32_t *>(w + o_anc);
-    c->st_target = reinterpret_cast<int32_t *>(w + o_tgt);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     e = cudaMemsetAsync(c->ws, 0, off, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -999,21 +998,23 @@ dflash_status dflash_select_step_host(dflash_select_handle h, const void *hidden
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int L = c->cfg.L;
     const size_t nb = static_cast<size_t>(B);
-    // the previous call returned once its walkers had finished, after the
-    // step's uploads: the pinned image is free
+    // anchor and target are read by the kernels from the handle's mapped
+    // pinned image; the previous call returned once its walkers, the last
+    // readers of that image, had finished, so it is free
     uint8_t *const in_host = c->st_in_host;
-    const size_t tgt_off = reinterpret_cast<uint8_t *>(c->st_target) - reinterpret_cast<uint8_t *>(c->st_anchor);
+    const size_t tgt_off = c->st_tgt_off;
     std::memcpy(in_host, anchor_host, nb * 4);
     std::memcpy(in_host + tgt_off, target_host, nb * (L + 1) * 4);
+    const int32_t *anchor_dev = reinterpret_cast<const int32_t *>(c->st_in_dev);
+    const int32_t *target_dev = reinterpret_cast<const int32_t *>(c->st_in_dev + tgt_off);
     CUDA_TRY(cudaMemcpyAsync(c->st_hidden, hidden_host, nb * L * c->cfg.d * 2, cudaMemcpyHostToDevice, s));
-    CUDA_TRY(cudaMemcpyAsync(c->st_anchor, in_host, tgt_off + nb * (L + 1) * 4, cudaMemcpyHostToDevice, s));
     // the walkers write the results, a copy of the error word and a flag per
     // sequence straight into the mapped block
     const uint32_t step = ++c->host_step;
     c->hs_done = c->hd_done;
     c->hs_err_snap = c->hd_err;
     c->hs_step = step;
-    dflash_status st = dflash_select_run_verify(h, c->st_hidden, c->st_anchor, B, c->st_target, c->hd_path,
+    dflash_status st = dflash_select_run_verify(h, c->st_hidden, anchor_dev, B, target_dev, c->hd_path,
                                                 c->hd_accept, c->hd_emitted, nullptr, nullptr, nullptr, nullptr,
                                                 nullptr, stream);
     c->hs_done = nullptr;

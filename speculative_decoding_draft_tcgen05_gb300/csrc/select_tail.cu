@@ -153,6 +153,9 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
             tma_load_2d(st + kWTileBytes, &p.tm_wb, k0 + s * 64, 0, bar_full + 8u * s, pol);
         }
     }
+    // the anchor is an input of the run, not written by the previous kernel
+    // (it may sit in mapped host memory): read before the dependency wait
+    const int32_t anchor_tok = (t == 0 && tid == 32) ? p.anchor[b] : 0;
     pdl_wait();
 
     // ---------------- 1. candidates of t and t-1 from the partial lists
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
     if (t == 0 && warp == 1 && lane < K) {
         int32_t a = -1;
         if (lane == 0) {
-            a = p.anchor[b];
+            a = anchor_tok;
             if (a < 0 || static_cast<int64_t>(a) >= p.V) {
                 atomicOr(p.err, DEV_ERR_TOKEN);
                 a = 0;

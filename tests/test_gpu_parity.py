@@ -236,6 +236,34 @@ def test_step_host_bound_pageable_and_error(pkg):
         assert path.numpy().tolist() == full["path"].tolist()
 
 
+@pytest.mark.parametrize("B", [40, 3])
+def test_step_host_equals_run_verify(pkg, B):
+    """The host step (anchor and target read from mapped host memory, results
+    written there by the walking kernel) equals the device-buffer run with
+    the accept check, on the three-kernel tail (B = 40) and the fused one."""
+    inp = wl.make_inputs(wl.custom(name="edge", seed=23, std_w=0.05, B=B, L=7, K=16, V=2000, d=128))
+    d = parity.to_device(inp, "cuda")
+    w = inp.wl
+    tgt = torch.randint(0, w.V, (B, w.L + 1), generator=torch.Generator().manual_seed(3), dtype=torch.int32)
+    with pkg.Selector(d["W"], d["E"], d["W_A"], d["W_B"], d["W_H"], L=w.L, K=w.K, max_batch=B) as sel:
+        out = sel.outputs(B, full=False)
+        acc_d = torch.empty(B, dtype=torch.int32, device="cuda")
+        em_d = torch.empty(B, w.L + 1, dtype=torch.int32, device="cuda")
+        step = pkg.bind_step(sel.h, d["hidden"], d["anchor"], out["path"], target=tgt.cuda(), accept_len=acc_d,
+                             emitted=em_d)
+        step()
+        pkg.dflash_select_sync_status(sel.h)
+        path_h = torch.empty(B, w.L, dtype=torch.int32).pin_memory()
+        acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
+        em_h = torch.empty(B, w.L + 1, dtype=torch.int32).pin_memory()
+        host = pkg.bind_step_host(sel.h, inp.hidden.pin_memory(), inp.anchor.pin_memory(), tgt.pin_memory(),
+                                  path_h, acc_h, em_h)
+        for _ in range(3):
+            host()
+            assert torch.equal(path_h, out["path"].cpu())
+            assert torch.equal(acc_h, acc_d.cpu()) and torch.equal(em_h, em_d.cpu())
+
+
 def test_profile_records_kernels(pkg):
     inp = parity.inputs_for("tiny")
     d = parity.to_device(inp, "cuda")
