@@ -60,7 +60,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint
 {
     extern __shared__ uint64_t mlists[];  // [G][K]
     __shared__ uint64_t wl[kMergeWarps][32];
-    pdl_trigger();
     pdl_wait();
     const int col = blockIdx.x;
     if (threadIdx.x == 0) thr_g[col] = 0;  // ready for the next lm_head pass
@@ -82,6 +81,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_kernel(const uint
         }
     }
     __syncthreads();
+    // the next kernel (the projections) is scheduled once the lists are in
+    // shared memory: its early weight loads no longer compete with these
+    // (measured: 1.3 us per batch-8 step)
+    pdl_trigger();
     // Fast path: K lists whose best logits are all >= v hold K keys of logit
     // >= v, so the K-th best key is at least (v, any id) and only keys of logit
     // >= v can be in the result (v: the K-th largest best logit among the
@@ -157,7 +160,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_small_kernel(
     const uint64_t *__restrict__ part, int G, int N, int K, int32_t *ids_ws, float *vals_ws, int32_t *ids_out,
     float *vals_out, uint64_t *thr_g, uint64_t *keys_out, const DedupParams dd)
 {
-    pdl_trigger();
     pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int col = blockIdx.x * kMergeWarps + warp;
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) topk_merge_small_kernel(
 #pragma unroll
     for (int g = 0; g < 32; ++g)
         if (g < G) run = list_merge(run, x[g], lane, K);
+    pdl_trigger();  // the lists are read (warps past N count as triggered when they exit)
     merge_emit(col, run, lane, K, ids_ws, vals_ws, ids_out, vals_out, keys_out, dd, lane == 0);
 }
 
