@@ -22,8 +22,9 @@
 //      mma.sync, fp32 accumulation;
 //   4. the partials are summed over the cluster in rank order through DSMEM,
 //      each CTA owning 256/CS columns of A and B; A is multiplied by g_t and
-//      each CTA forms its partial pair dot products; rank 0 sums those (rank
-//      order) and adds U_t(b): the table S_t;
+//      each CTA forms its partial pair dot products and stores them into rank
+//      0's shared memory; rank 0 sums those (rank order) and adds U_t(b): the
+//      table S_t;
 //   5. the last cluster of a sequence (atomic ticket, no waiting) walks.
 // With precomputed tables [A(v) | B(v)] for every token (a handle option),
 // steps 1 and 3 are replaced by a gather: each CTA reads its 256/cs columns of
@@ -50,8 +51,10 @@ __host__ __device__ inline uint32_t tail_stage_bytes(int K)
 }
 
 struct TailLayout {
-    uint32_t stage, off_mlist, off_ctalist, off_pp, off_bar, off_misc, total;
+    uint32_t stage, off_mlist, off_ctalist, off_bar, off_misc, total;
 };
+
+
 
 __host__ __device__ inline TailLayout tail_layout(int K, int S, int G, int cs)
 {
@@ -60,8 +63,7 @@ __host__ __device__ inline TailLayout tail_layout(int K, int S, int G, int cs)
     const int per = (G + cs - 1) / cs;
     l.off_mlist = S * l.stage;
     l.off_ctalist = l.off_mlist + static_cast<uint32_t>(2 * per * K) * 8;
-    l.off_pp = l.off_ctalist + 2 * 32 * 8;
-    l.off_bar = l.off_pp + static_cast<uint32_t>(K * K) * 4;
+    l.off_bar = l.off_ctalist + 2 * 32 * 8;
     l.off_misc = l.off_bar + 8 * S;
     l.total = l.off_misc + 16;
     return l;
@@ -130,7 +132,6 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
     const TailLayout lay = tail_layout(K, S, G, cs);
     uint64_t *const mlist = reinterpret_cast<uint64_t *>(gbase + lay.off_mlist);
     uint64_t *const cta_list = reinterpret_cast<uint64_t *>(gbase + lay.off_ctalist);
-    float *const Pp = reinterpret_cast<float *>(gbase + lay.off_pp);
     const uint32_t bar_full = base + lay.off_bar;
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(gbase + lay.off_misc);
 
@@ -410,6 +411,14 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
         }
     }
     __syncthreads();
+    // each CTA's partial pair dots go straight to its slot in rank 0's receive
+    // area [CS][K * K]: in rank 0's stage buffers past its partial projections
+    // and its reduced slice (which other CTAs read before they write here; no
+    // MMA or copy of a stage is pending anywhere by now)
+    const uint32_t rx_off = (tab ? 0u : static_cast<uint32_t>(2 * K * (kEmbed + 4) * 4)) +
+                            (static_cast<uint32_t>(2 * K * rs * 4) + 15u) / 16u * 16u;
+    float *const rx = reinterpret_cast<float *>(gbase + rx_off);
+    float *const rx_slot = cluster.map_shared_rank(rx, 0) + rank * K * K;
     for (int pr = tid; pr < K * K; pr += 256) {
         const int i = pr / K, j = pr % K;
         const float *a = Red + i * rs;
@@ -421,30 +430,24 @@ __global__ void __launch_bounds__(256, 1) select_tail_kernel(const __grid_consta
             d1 = fmaf(a[e + 1], bb[e + 1], d1);
         }
         if (e < es) d0 = fmaf(a[e], bb[e], d0);
-        Pp[pr] = d0 + d1;
+        rx_slot[pr] = d0 + d1;
     }
-    cluster.sync();
+    cluster.sync();  // the partials are in place; no CTA reads another CTA's shared memory after this
+    if (rank != 0) return;
 
-    // ---------------- 4. rank 0: the table S_t
-    if (rank == 0) {
+    // ---------------- 4. rank 0: the table S_t, its partials summed in rank order
+    {
         float *Pt = p.P + static_cast<size_t>(pos) * K * K;
         float *Po = p.P_out ? p.P_out + static_cast<size_t>(pos) * K * K : nullptr;
         for (int pr = tid; pr < K * K; pr += 256) {
             const int i = pr / K, j = pr % K;
-            float v[8];
-#pragma unroll
-            for (int qq = 0; qq < 8; ++qq) v[qq] = (qq < cs) ? cluster.map_shared_rank(Pp, qq)[pr] : 0.f;
-            float sum = v[0];
-#pragma unroll
-            for (int qq = 1; qq < 8; ++qq)
-                if (qq < cs) sum += v[qq];
+            float sum = rx[pr];
+            for (int qq = 1; qq < cs; ++qq) sum += rx[qq * K * K + pr];
             const float sc = (t == 0 && i > 0) ? -INFINITY : cand_val[j] + sum;
             Pt[pr] = sc;
             if (Po) Po[pr] = sc;
         }
     }
-    cluster.sync();  // every CTA's shared memory stays alive until rank 0 has read it
-    if (rank != 0) return;
 
     // ---------------- 5. the last cluster of the sequence walks
     __syncthreads();
@@ -501,7 +504,9 @@ int tail_stages(int K, int G, int cs, int smem_optin)
         const size_t reuse = static_cast<size_t>(2 * K) * (kEmbed + 4) * 4 +
                              static_cast<size_t>(2 * K) * (kEmbed / cs + kRedPad) * 4;
         const size_t walk = static_cast<size_t>(16) * K * K * 4;
-        if (reuse > static_cast<size_t>(S) * l.stage || walk > static_cast<size_t>(S) * l.stage) continue;
+        // rank 0 receives the CS CTAs' partial pair dots after those two
+        const size_t rx_end = reuse + 16 + static_cast<size_t>(cs) * K * K * 4;
+        if (rx_end > static_cast<size_t>(S) * l.stage || walk > static_cast<size_t>(S) * l.stage) continue;
         if (l.total + 1024 + 10 * 1024 <= static_cast<size_t>(smem_optin)) return S;  // 10 KB: static shared memory
     }
     return 0;
