@@ -160,6 +160,7 @@ struct dflash_select_ctx {
     const void *W, *E, *WA, *WB, *WH;
     int device = 0, num_sms = 0;
     size_t smem_optin = 0;  // opt-in shared memory per block
+    size_t smem_per_sm = 0;
     CUtensorMap tm_w, tm_gate, tm_h, tm_wa, tm_wb;
     CUtensorMap tm_pa[3], tm_pb[3];  // W_A, W_B with 64 x {64, 128, 256}-row boxes (projection tiles)
     const void *h_ptr = nullptr, *hp_ptr = nullptr;
@@ -410,6 +411,7 @@ static dflash_status init_impl(const dflash_select_config *cfg, const void *W_lm
     c->device = dev;
     c->num_sms = prop.multiProcessorCount;
     c->smem_optin = prop.sharedMemPerBlockOptin;
+    c->smem_per_sm = prop.sharedMemPerMultiprocessor;
     c->shard_v0 = v0;
     c->shard_rows = rows;
     c->m_tiles_vocab = static_cast<int>((rows + dfl::kLmTileM - 1) / dfl::kLmTileM);
@@ -754,8 +756,10 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
     }
     int slot = 1;  // profiling slots are filled in launch order
     prof_begin(c, slot, s);
+    // one position per CTA: at most a wave spreads over the GPU, one CTA per SM
+    const size_t spread = pl.N <= c->num_sms ? dfl::one_cta_per_sm_smem(c->smem_per_sm) : 0;
     CUDA_TRY(dfl::launch_topk_merge(part, G, pl.N, c->cfg.K, c->ids, c->vals, topk_ids, topk_vals, c->thr_g, s,
-                                    nullptr, dd));
+                                    nullptr, dd, spread));
     prof_end(c, slot++, 1, s);
     if (dd.tab) {
         prof_begin(c, slot, s);
@@ -827,7 +831,7 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
     q.err_snap = c->hs_err_snap;
     q.step = c->hs_step;
     prof_begin(c, slot, s);
-    CUDA_TRY(dfl::launch_pair_walk(q, s));
+    CUDA_TRY(dfl::launch_pair_walk(q, s, spread));  // one CTA per (sequence, position), as the merge
     prof_end(c, slot, 3, s);
     if (prof_on(c)) ++c->prof_runs;
     return ok();

@@ -223,9 +223,10 @@ cudaError_t prepare_pair_walk(int smem_optin)
     return set_max_dynamic_smem(pair_walk_kernel<32>, smem_optin);
 }
 
-cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s)
+cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s, size_t min_smem)
 {
-    const size_t smem = 2u * kEmbed * p.K * sizeof(float);
+    const size_t need = 2u * kEmbed * p.K * sizeof(float);
+    const size_t smem = need > min_smem ? need : min_smem;
     if (p.K == 16) return launch_ex(pair_walk_kernel<16>, dim3(p.B * p.L), dim3(256), smem, s, 1, p);
     return launch_ex(pair_walk_kernel<32>, dim3(p.B * p.L), dim3(256), smem, s, 1, p);
 }

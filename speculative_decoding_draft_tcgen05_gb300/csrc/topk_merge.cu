@@ -189,12 +189,13 @@ cudaError_t prepare_topk_merge(int smem_optin)
 
 cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws, float *vals_ws,
                               int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s, uint64_t *keys_out,
-                              const DedupParams &dd)
+                              const DedupParams &dd, size_t min_smem)
 {
     if (G <= 32)
         return launch_ex(topk_merge_small_kernel, dim3((N + kMergeWarps - 1) / kMergeWarps), dim3(kMergeWarps * 32), 0,
                          s, 1, part, G, N, K, ids_ws, vals_ws, ids_out, vals_out, thr_g, keys_out, dd);
-    const size_t smem = static_cast<size_t>(G) * K * sizeof(uint64_t);
+    const size_t need = static_cast<size_t>(G) * K * sizeof(uint64_t);
+    const size_t smem = need > min_smem ? need : min_smem;
     if (K == 16)
         return launch_ex(topk_merge_kernel<16>, dim3(N), dim3(kMergeWarps * 32), smem, s, 1, part, G, N, ids_ws,
                          vals_ws, ids_out, vals_out, thr_g, keys_out, dd);
