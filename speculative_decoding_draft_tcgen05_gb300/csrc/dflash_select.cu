@@ -756,8 +756,11 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
     }
     int slot = 1;  // profiling slots are filled in launch order
     prof_begin(c, slot, s);
-    // one position per CTA: at most a wave spreads over the GPU, one CTA per SM
-    const size_t spread = pl.N <= c->num_sms ? dfl::one_cta_per_sm_smem(c->smem_per_sm) : 0;
+    // one position per CTA: one or two waves spread over the GPU, at most one
+    // or two CTAs per SM
+    const size_t spread = pl.N <= c->num_sms       ? dfl::ctas_per_sm_smem(c->smem_per_sm, 1)
+                          : pl.N <= 2 * c->num_sms ? dfl::ctas_per_sm_smem(c->smem_per_sm, 2)
+                                                   : 0;
     CUDA_TRY(dfl::launch_topk_merge(part, G, pl.N, c->cfg.K, c->ids, c->vals, topk_ids, topk_vals, c->thr_g, s,
                                     nullptr, dd, spread));
     prof_end(c, slot++, 1, s);

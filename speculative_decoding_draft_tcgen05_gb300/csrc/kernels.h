@@ -56,13 +56,13 @@ cudaError_t set_max_dynamic_smem(void (*kern)(KArgs...), int smem_optin)
                                 smem_optin - static_cast<int>(fa.sharedSizeBytes));
 }
 
-// Dynamic shared memory that keeps a kernel to one CTA per SM (more than half
-// of an SM's shared memory). A grid of at most one wave that is launched
-// early (programmatic dependent launch) would otherwise crowd onto the SMs
-// its predecessor leaves free; reserving this spreads it over the whole GPU
-// as the predecessor's CTAs exit (measured: the pair tables and the merge at
-// batch 8, 3.1 us per step).
-inline size_t one_cta_per_sm_smem(size_t smem_per_sm) { return smem_per_sm / 2 + 1024; }
+// Dynamic shared memory that keeps a kernel to at most n CTAs per SM (more
+// than 1 / (n + 1) of an SM's shared memory). A grid of at most n waves that
+// is launched early (programmatic dependent launch) would otherwise crowd onto
+// the SMs its predecessor leaves free; reserving this spreads it over the
+// whole GPU as the predecessor's CTAs exit (measured on the merge and the pair
+// tables: 3.1 us per step at batch 8 with n = 1, 2.5 us at batch 32 with n = 2).
+inline size_t ctas_per_sm_smem(size_t smem_per_sm, int n) { return smem_per_sm / (n + 1) + 1024; }
 
 // Sets the shared-memory opt-ins of every kernel on the current device
 // (smem_optin = cudaDevAttrMaxSharedMemoryPerBlockOptin).
@@ -140,7 +140,7 @@ cudaError_t launch_dedup_compact(const DedupParams &d, const int32_t *ids, int R
 // same [G][N][K] layout) into the sorted top-K of each position; keys_out
 // (optional) receives the merged keys [N][K]; with dd.tab the merged
 // candidates (and the anchors) are marked for deduplication.
-// min_smem: dynamic shared memory to reserve at least (see one_cta_per_sm_smem).
+// min_smem: dynamic shared memory to reserve at least (see ctas_per_sm_smem).
 cudaError_t launch_topk_merge(const uint64_t *part, int G, int N, int K, int32_t *ids_ws,
                               float *vals_ws, int32_t *ids_out, float *vals_out, uint64_t *thr_g, cudaStream_t s,
                               uint64_t *keys_out = nullptr, const DedupParams &dd = DedupParams(),
@@ -203,7 +203,7 @@ struct PairParams {
     int *err_snap = nullptr;           // [B] host-mapped copies of the error word
     uint32_t step = 0;
 };
-// min_smem: dynamic shared memory to reserve at least (see one_cta_per_sm_smem).
+// min_smem: dynamic shared memory to reserve at least (see ctas_per_sm_smem).
 cudaError_t launch_pair_walk(const PairParams &p, cudaStream_t s, size_t min_smem = 0);
 
 // ---- fused tail for small batches: merge + projections + pair tables + walk ----
