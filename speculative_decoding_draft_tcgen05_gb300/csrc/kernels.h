@@ -56,14 +56,6 @@ cudaError_t set_max_dynamic_smem(void (*kern)(KArgs...), int smem_optin)
                                 smem_optin - static_cast<int>(fa.sharedSizeBytes));
 }
 
-// Dynamic shared memory that keeps a kernel to at most n CTAs per SM (more
-// than 1 / (n + 1) of an SM's shared memory). A grid of at most n waves that
-// is launched early (programmatic dependent launch) would otherwise crowd onto
-// the SMs its predecessor leaves free; reserving this spreads it over the
-// whole GPU as the predecessor's CTAs exit (measured on the merge and the pair
-// tables: 3.1 us per step at batch 8 with n = 1, 2.5 us at batch 32 with n = 2).
-inline size_t ctas_per_sm_smem(size_t smem_per_sm, int n) { return smem_per_sm / (n + 1) + 1024; }
-
 // Sets the shared-memory opt-ins of every kernel on the current device
 // (smem_optin = cudaDevAttrMaxSharedMemoryPerBlockOptin).
 cudaError_t prepare_lmhead(int smem_optin);
@@ -135,6 +127,14 @@ struct DedupParams {
 };
 // uniq / rep from the marks, one thread per gathered row (R_total rows).
 cudaError_t launch_dedup_compact(const DedupParams &d, const int32_t *ids, int R_total, cudaStream_t s);
+
+// Dynamic shared memory that keeps a kernel to at most n CTAs per SM (more
+// than 1 / (n + 1) of an SM's shared memory). A grid of at most n waves that
+// is launched early (programmatic dependent launch) would otherwise crowd onto
+// the SMs its predecessor leaves free; reserving this spreads it over the
+// whole GPU as the predecessor's CTAs exit (measured on the merge and the pair
+// tables: 3.1 us per step at batch 8 with n = 1, 2.5 us at batch 32 with n = 2).
+inline size_t ctas_per_sm_smem(size_t smem_per_sm, int n) { return smem_per_sm / (n + 1) + 1024; }
 
 // Merges the partial lists of every CTA (or of every vocabulary shard: the
 // same [G][N][K] layout) into the sorted top-K of each position; keys_out
