@@ -200,7 +200,6 @@ __global__ void __launch_bounds__(kRejThreads) verify_rejection_kernel(
     int64_t V, int32_t *__restrict__ accept, int32_t *__restrict__ emitted)
 {
     __shared__ RejShared s;
-    pdl_trigger();
     pdl_wait();
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
@@ -282,6 +281,9 @@ __global__ void __launch_bounds__(kRejThreads) verify_rejection_kernel(
         }
     }
     cluster.sync();  // the only one: no CTA touches another's shared memory after it
+    // the rows are read: the next kernel (the next lm_head pass) may be
+    // scheduled without its early weight loads competing with those reads
+    pdl_trigger();
 
     if (warp == 0) {  // every CTA: Z, the target and the CTA that holds it (the same arithmetic everywhere)
         const uint64_t mp = lane < C ? s.tot_p[lane] : 0ull;
