@@ -374,18 +374,28 @@ cudaError_t launch_verify_rejection(const int32_t *path, const int32_t *ids, con
                                     const float *u_acc, const float *u_res, int B, int L, int K, int64_t V,
                                     int32_t *accept, int32_t *emitted, cudaStream_t s)
 {
-    // per device, once: the SM count and the opt-in to clusters of 16
-    static std::atomic<int> sms_of[64];
+    // per device, once: the SM count, the shared memory that keeps one CTA per
+    // SM, and the opt-ins to clusters of 16 and to that much shared memory
+    static std::atomic<int> sms_of[64], spread_of[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int sms = (dev >= 0 && dev < 64) ? sms_of[dev].load(std::memory_order_relaxed) : 0;
+    int sms = (dev >= 0 && dev < 64) ? sms_of[dev].load(std::memory_order_acquire) : 0;
+    int spread = (sms != 0) ? spread_of[dev].load(std::memory_order_relaxed) : 0;
     if (sms == 0) {
+        int per_sm = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(verify_rejection_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        spread = static_cast<int>(ctas_per_sm_smem(static_cast<size_t>(per_sm), 1));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(verify_rejection_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, spread);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) sms_of[dev].store(sms, std::memory_order_relaxed);
+        if (dev >= 0 && dev < 64) {
+            spread_of[dev].store(spread, std::memory_order_relaxed);
+            sms_of[dev].store(sms, std::memory_order_release);  // publishes spread
+        }
     }
 #ifndef DFL_REJ_FIXED_C
     // CTAs per sequence: 16 for up to 4 sequences (clusters of 16 need a whole
@@ -395,7 +405,11 @@ cudaError_t launch_verify_rejection(const int32_t *path, const int32_t *ids, con
 #else
     const int C = DFL_REJ_FIXED_C;
 #endif
-    return launch_ex(verify_rejection_kernel, dim3(B, 1, C), dim3(kRejThreads), 0, s, C, path, ids, q, p, u_acc,
+    // While all CTAs fit one per SM, reserved (unused) shared memory keeps two of
+    // these 1024-thread CTAs from sharing an SM when the kernel is scheduled
+    // early, beside its predecessor's last CTAs.
+    const size_t smem = (static_cast<int64_t>(C) * B <= sms) ? static_cast<size_t>(spread) : 0;
+    return launch_ex(verify_rejection_kernel, dim3(B, 1, C), dim3(kRejThreads), smem, s, C, path, ids, q, p, u_acc,
                      u_res, L, K, V, accept, emitted);
 }
 
