@@ -375,6 +375,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv2_kernel(const __grid_con
 constexpr int kSmallThreads = 256;
 constexpr int kSmallAcc = 64;   // PM * 2 NG accumulators per thread
 constexpr int kSmallRows = 8;   // the few-row kernel's limit (measured: beyond 8 rows the tcgen05 kernel is faster)
+constexpr int kSmallUnits = 2;  // 16-byte pieces of d per thread whose x loads are in flight together
 
 // 1D bulk copy global -> this CTA's shared memory, counted on `bar` in bytes.
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
@@ -385,7 +386,7 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
 }
 
 template <int PM, int NG>
-__global__ void __launch_bounds__(kSmallThreads) conv2_small_kernel(const __nv_bfloat16 *__restrict__ x,
+__global__ void __launch_bounds__(kSmallThreads, 2) conv2_small_kernel(const __nv_bfloat16 *__restrict__ x,
                                                                     const __nv_bfloat16 *__restrict__ base,
                                                                     const __nv_bfloat16 *__restrict__ Wc,
                                                                     __nv_bfloat16 *__restrict__ y, int P, int S, int d,
@@ -419,9 +420,8 @@ __global__ void __launch_bounds__(kSmallThreads) conv2_small_kernel(const __nv_b
     const int eh = tid & 1, eg = (tid >> 1) % NG, er = tid / (2 * NG);
     const bool epi = er < P && eg < ng;
     const size_t ch = static_cast<size_t>(g0 + (epi ? eg : 0)) * 16 + 8 * eh;
-    float b0[8], b1[8];
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(base + ch)), b0);
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(base + d + ch)), b1);
+    const uint4 bv0 = __ldg(reinterpret_cast<const uint4 *>(base + ch));
+    const uint4 bv1 = __ldg(reinterpret_cast<const uint4 *>(base + d + ch));
     pdl_trigger();
     pdl_wait();
     uint4 xv = make_uint4(0u, 0u, 0u, 0u), pv = make_uint4(0u, 0u, 0u, 0u);
@@ -441,20 +441,38 @@ __global__ void __launch_bounds__(kSmallThreads) conv2_small_kernel(const __nv_b
 #pragma unroll
         for (int q = 0; q < 2 * NG; ++q) acc[r][q] = 0.f;
     const uint4 *w4 = reinterpret_cast<const uint4 *>(wsm);
-    for (int u = tid; u < nu; u += kSmallThreads) {
-        float fw[2 * NG][8];
+    // kSmallUnits pieces of d per thread and pass, every x load of a pass issued
+    // before its first use (one round trip to L2 per pass; d <= 4096 is one
+    // pass); the sums still run over u in increasing order
+    for (int u0 = tid; u0 < nu; u0 += kSmallUnits * kSmallThreads) {
+        uint4 xr[kSmallUnits][PM];
 #pragma unroll
-        for (int q = 0; q < 2 * NG; ++q) bf16x8_to_f32(q < 2 * ng ? w4[q * nu + u] : make_uint4(0u, 0u, 0u, 0u), fw[q]);
+        for (int v = 0; v < kSmallUnits; ++v) {
+            const int u = u0 + v * kSmallThreads;
 #pragma unroll
-        for (int r = 0; r < PM; ++r) {
-            if (r >= P) break;
-            float fx[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(x + static_cast<size_t>(r) * d + 8 * static_cast<size_t>(u)),
-                          fx);
+            for (int r = 0; r < PM; ++r)
+                xr[v][r] = (u < nu && r < P) ? *reinterpret_cast<const uint4 *>(x + static_cast<size_t>(r) * d +
+                                                                                  8 * static_cast<size_t>(u))
+                                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int v = 0; v < kSmallUnits; ++v) {
+            const int u = u0 + v * kSmallThreads;
+            if (u >= nu) break;
+            float fw[2 * NG][8];
 #pragma unroll
             for (int q = 0; q < 2 * NG; ++q)
+                bf16x8_to_f32(q < 2 * ng ? w4[q * nu + u] : make_uint4(0u, 0u, 0u, 0u), fw[q]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) acc[r][q] = fmaf(fw[q][k], fx[k], acc[r][q]);
+            for (int r = 0; r < PM; ++r) {
+                if (r >= P) break;
+                float fx[8];
+                bf16x8_to_f32(xr[v][r], fx);
+#pragma unroll
+                for (int q = 0; q < 2 * NG; ++q)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) acc[r][q] = fmaf(fw[q][k], fx[k], acc[r][q]);
+            }
         }
     }
 #pragma unroll
@@ -476,7 +494,9 @@ __global__ void __launch_bounds__(kSmallThreads) conv2_small_kernel(const __nv_b
     __syncthreads();
     if (epi) {
         const float c0 = corr[er * 2 * NG + 2 * eg], c1 = corr[er * 2 * NG + 2 * eg + 1];
-        float fx[8], fp[8];
+        float fx[8], fp[8], b0[8], b1[8];
+        bf16x8_to_f32(bv0, b0);
+        bf16x8_to_f32(bv1, b1);
         bf16x8_to_f32(xv, fx);
         bf16x8_to_f32(pv, fp);
         uint32_t out[4];
