@@ -375,7 +375,10 @@ __global__ void __launch_bounds__(kConvThreads, 1) conv2_kernel(const __grid_con
 constexpr int kSmallThreads = 256;
 constexpr int kSmallAcc = 64;   // PM * 2 NG accumulators per thread
 constexpr int kSmallRows = 8;   // the few-row kernel's limit (measured: beyond 8 rows the tcgen05 kernel is faster)
-constexpr int kSmallUnits = 2;  // 16-byte pieces of d per thread whose x loads are in flight together
+// 16-byte pieces of d per thread whose x loads are in flight together: two up
+// to d = 4096 (one pass; two CTAs per SM), else one (three CTAs per SM keep the
+// 2 d / 32 CTAs of a larger d in one wave)
+constexpr int kSmallUnitsMaxD = 4096;
 
 // 1D bulk copy global -> this CTA's shared memory, counted on `bar` in bytes.
 __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
@@ -385,8 +388,8 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
                  : "memory");
 }
 
-template <int PM, int NG>
-__global__ void __launch_bounds__(kSmallThreads, 2) conv2_small_kernel(const __nv_bfloat16 *__restrict__ x,
+template <int PM, int NG, int UPT>
+__global__ void __launch_bounds__(kSmallThreads, (UPT > 1) ? 2 : 3) conv2_small_kernel(const __nv_bfloat16 *__restrict__ x,
                                                                     const __nv_bfloat16 *__restrict__ base,
                                                                     const __nv_bfloat16 *__restrict__ Wc,
                                                                     __nv_bfloat16 *__restrict__ y, int P, int S, int d,
@@ -441,13 +444,13 @@ __global__ void __launch_bounds__(kSmallThreads, 2) conv2_small_kernel(const __n
 #pragma unroll
         for (int q = 0; q < 2 * NG; ++q) acc[r][q] = 0.f;
     const uint4 *w4 = reinterpret_cast<const uint4 *>(wsm);
-    // kSmallUnits pieces of d per thread and pass, every x load of a pass issued
-    // before its first use (one round trip to L2 per pass; d <= 4096 is one
-    // pass); the sums still run over u in increasing order
-    for (int u0 = tid; u0 < nu; u0 += kSmallUnits * kSmallThreads) {
-        uint4 xr[kSmallUnits][PM];
+    // UPT pieces of d per thread and pass, every x load of a pass issued before
+    // its first use (one round trip to L2 per pass); the sums still run over u
+    // in increasing order
+    for (int u0 = tid; u0 < nu; u0 += UPT * kSmallThreads) {
+        uint4 xr[UPT][PM];
 #pragma unroll
-        for (int v = 0; v < kSmallUnits; ++v) {
+        for (int v = 0; v < UPT; ++v) {
             const int u = u0 + v * kSmallThreads;
 #pragma unroll
             for (int r = 0; r < PM; ++r)
@@ -456,7 +459,7 @@ __global__ void __launch_bounds__(kSmallThreads, 2) conv2_small_kernel(const __n
                                              : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int v = 0; v < kSmallUnits; ++v) {
+        for (int v = 0; v < UPT; ++v) {
             const int u = u0 + v * kSmallThreads;
             if (u >= nu) break;
             float fw[2 * NG][8];
@@ -512,20 +515,23 @@ __global__ void __launch_bounds__(kSmallThreads, 2) conv2_small_kernel(const __n
     if (timed_out && tid == 0) atomicOr(err, DEV_ERR_TIMEOUT);
 }
 
-template <int PM, int NG>
+template <int PM, int NG, int UPT>
 cudaError_t launch_small(const __nv_bfloat16 *x, const __nv_bfloat16 *base, const __nv_bfloat16 *Wc, __nv_bfloat16 *y,
                          int P, int S, int d, int *err, cudaStream_t s)
 {
     const size_t smem = static_cast<size_t>(2 * NG) * d * 2;
     const int G = d / 16;
-    return launch_ex(conv2_small_kernel<PM, NG>, dim3((G + NG - 1) / NG), dim3(kSmallThreads), smem, s, 1, x, base, Wc,
+    return launch_ex(conv2_small_kernel<PM, NG, UPT>, dim3((G + NG - 1) / NG), dim3(kSmallThreads), smem, s, 1, x, base, Wc,
                      y, P, S, d, err);
 }
 
 // Lets the few-row kernel take the Wc rows it needs (up to 64 KB).
 cudaError_t prepare_small()
 {
-    return cudaFuncSetAttribute(conv2_small_kernel<kSmallRows, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(conv2_small_kernel<kSmallRows, 1, 2>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(conv2_small_kernel<kSmallRows, 1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 64 * 1024);
 }
 
@@ -616,10 +622,14 @@ extern "C" dflash_status dflash_conv2_run(dflash_conv2_handle h, const void *X, 
     const int P = static_cast<int>(P64);
 
     if (P <= dfl::kSmallRows) {  // a matrix-vector product: CUDA cores, one channel group per CTA
-        const cudaError_t e = dfl::launch_small<dfl::kSmallRows, 1>(
-            static_cast<const __nv_bfloat16 *>(X), static_cast<const __nv_bfloat16 *>(h->base),
-            static_cast<const __nv_bfloat16 *>(h->Wc), static_cast<__nv_bfloat16 *>(Y), P, S, d, h->err,
-            static_cast<cudaStream_t>(stream));
+        const auto *x = static_cast<const __nv_bfloat16 *>(X);
+        const auto *base = static_cast<const __nv_bfloat16 *>(h->base);
+        const auto *Wc = static_cast<const __nv_bfloat16 *>(h->Wc);
+        auto *y = static_cast<__nv_bfloat16 *>(Y);
+        const auto st = static_cast<cudaStream_t>(stream);
+        const cudaError_t e = (d <= dfl::kSmallUnitsMaxD)
+                                  ? dfl::launch_small<dfl::kSmallRows, 1, 2>(x, base, Wc, y, P, S, d, h->err, st)
+                                  : dfl::launch_small<dfl::kSmallRows, 1, 1>(x, base, Wc, y, P, S, d, h->err, st);
         if (e != cudaSuccess) return conv_fail(DFLASH_ERR_CUDA, "convolution launch failed (error %lld)", e);
         return DFLASH_OK;
     }
