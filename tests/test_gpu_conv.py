@@ -46,6 +46,8 @@ def _check(gpu, ref):
     # up to 8 rows: the CUDA-core kernel
     (1, 8, 128),      # one block, d = 128
     (1, 8, 2560),     # Qwen3-4B width, one block
+    (1, 8, 4096),     # the widest d with two 16-byte pieces per thread (one pass)
+    (1, 7, 4160),     # the narrowest d with one piece per thread (three passes)
     (1, 8, 5120),     # 27B-class width
     (3, 1, 256),      # S = 1: every row starts a block
     (1, 5, 16384),    # the widest d (64 KB of Wc rows per CTA)
