@@ -636,20 +636,35 @@ extern "C" dflash_status dflash_conv2_run(dflash_conv2_handle h, const void *X, 
 
     dfl::ConvParams prm;
     const int m_tiles = (h->rows + dfl::kConvTileM - 1) / dfl::kConvTileM;
-    // Spread the work over the SMs: first narrower position tiles (down to 16),
-    // then, with 16-wide tiles, d split over a cluster -- each while the grid
-    // stays within one CTA per SM.
-    int NT = P <= 256 ? ((P + 15) / 16) * 16 : 256;
-    while (NT > 16) {
-        const int half = ((NT / 2 + 15) / 16) * 16;
-        if (static_cast<int64_t>(m_tiles) * ((P + half - 1) / half) > h->num_sms) break;
-        NT = half;
+    // The position-tile width NT (halved from the rows, down to 16) and the
+    // split of d over a cluster (ks of 1, 2, 4, 8 dividing the k-blocks) that,
+    // within one CTA per SM and the shared memory, stream the fewest bytes per
+    // CTA: KB / ks stages of 16 KB of Wc and NT rows of X (a CTA's load time
+    // sets the call's length; narrower tiles re-read Wc once per tile).
+    // Ties go to the larger grid. With no pair in one wave: NT = 256, no split.
+    const int KB = d / dfl::kLmTileK;
+    int NT = 256, ks = 1;
+    {
+        int64_t best = -1, best_grid = 0;
+        for (int nt = P <= 256 ? ((P + 15) / 16) * 16 : 256;; nt = ((nt / 2 + 15) / 16) * 16) {
+            for (int k = 1; k <= dfl::kConvMaxSplit; k <<= 1) {
+                const int64_t grid = static_cast<int64_t>(m_tiles) * ((P + nt - 1) / nt) * k;
+                if (KB % k != 0 || grid > h->num_sms ||
+                    dfl::conv_layout(nt, k, 1).total + 1024u > static_cast<uint32_t>(h->smem_optin))
+                    continue;
+                const int64_t bytes = static_cast<int64_t>(KB / k) * dfl::conv_layout(nt, k, 1).stage_bytes;
+                if (best < 0 || bytes < best || (bytes == best && grid > best_grid)) {
+                    best = bytes;
+                    best_grid = grid;
+                    NT = nt;
+                    ks = k;
+                }
+            }
+            if (nt <= 16) break;
+        }
     }
     prm.NT = NT;
     const int n_tiles = (P + NT - 1) / NT;
-    const int KB = d / dfl::kLmTileK;
-    int ks = dfl::kConvMaxSplit;
-    while (ks > 1 && (KB % ks != 0 || static_cast<int64_t>(m_tiles) * n_tiles * ks > h->num_sms)) ks >>= 1;
     prm.ksplit = ks;
     const int KBc = KB / ks;
     int stages = KBc < dfl::kConvMaxStages ? KBc : dfl::kConvMaxStages;  // as deep as shared memory allows

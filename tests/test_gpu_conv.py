@@ -56,7 +56,8 @@ def _check(gpu, ref):
     (4, 8, 2560),     # 32 rows
     (3, 11, 1024),    # 33 rows: three 16-wide tiles
     (5, 7, 640),      # ragged rows, 80 Wc rows (one partial Wc tile)
-    (40, 8, 2560),    # 320 rows, three Wc tiles (the last ragged)
+    (40, 8, 2560),    # 320 rows, three Wc tiles (the last ragged): 64-wide tiles, d split over 8
+    (32, 8, 5120),    # 256 rows at the 27B-class width: 128-wide tiles, d split over 8
     (1, 300, 64),     # one long block, d = 64 (a single k-block, no split)
 ])
 def test_conv_matches_oracle(pkg, B, S, d):
