@@ -523,7 +523,7 @@ def run_ours(args):
     return 0
 
 
-CONVS_PER_FORWARD = 20  # before and after each attention and feed-forward sublayer of a five-layer drafter
+CONVS_PER_FORWARD = 20  # one in front of and one behind every attention and every feed-forward sublayer, five layers
 
 
 def run_conv(args):

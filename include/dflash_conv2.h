@@ -3,15 +3,15 @@
  * on one GB300 GPU.
  *
  * Blog post "DFlash 2: Keep Drafting Parallel", section "A Lightweight Local
- * Convolution": the drafter inserts, before and after each attention and
- * feed-forward sublayer, a depthwise convolution with two taps, one on the
- * current position and one on the position before it,
+ * Convolution": in front of and behind every attention and every feed-forward
+ * sublayer the drafter applies a two-tap depthwise convolution, one tap
+ * weighing the current position and the other the position before it,
  *     Conv_k(x)_t = k_{t,0} (.) x_t + k_{t,1} (.) x_{t-1},
  * whose coefficients are a learned base kernel plus a small correction
  * computed from the current hidden state, one correction per 16 channels. The
  * first draft position reads the last verified token's representation, each
- * later position its predecessor's; the convolution is block-local and
- * stateless.
+ * later position its predecessor's; nothing carries over from one block to
+ * the next.
  *
  * This library computes, for every block b and row t of X [B, S, d]:
  *     corr_{t,i}[g] = sum_j Wc[2g + i, j] * X[b, t, j]        (g = 0 .. d/16 - 1)

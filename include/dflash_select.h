@@ -135,12 +135,13 @@ dflash_status dflash_select_run_sampled(dflash_select_handle h, const void *hidd
                                         float *pair_scores, int32_t *path, float *draft_probs,
                                         float *path_score, uint8_t *tie_flags, void *stream);
 
-/* Rejection-sampling verification of a sampled draft (same section: rejection
- * sampling restores the exact target distribution). Draft token path[t] is
- * kept when u_acc[t] < min(1, p_t(x) / q_t(x)); at the first rejection the
- * emitted token is drawn from max(0, p_t - q_t) normalised (q_t is zero off
- * the candidates), by inverting its CDF in vocabulary order with u_res; when
- * all L drafts are kept the bonus token is drawn from p_L the same way.
+/* Rejection-sampling verification of a sampled draft (same section: verified
+ * by rejection sampling, the output follows the target's distribution
+ * exactly). Draft token path[t] is kept when u_acc[t] < min(1, p_t(x) /
+ * q_t(x)); at the first rejection the emitted token is drawn from
+ * max(0, p_t - q_t) normalised (q_t is zero off the candidates), by inverting
+ * its CDF in vocabulary order with u_res; when all L drafts are kept the bonus
+ * token is drawn from p_L the same way.
  *   path [B, L] int32, topk_ids [B, L, K] int32, draft_probs [B, L, K] fp32
  *   (as written by dflash_select_run_sampled)
  *   target_probs [B, L+1, V] fp32  target distribution after x0, path[0], ...

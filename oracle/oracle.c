@@ -25,7 +25,7 @@
  *       table E [V, d] and W_A, W_B, W_H of shape [e, d]; no bias, no norm.
  *   R2  U_t is the raw lm_head logit W[b] . h_t.
  *   R3  the walk is a max-sum (Viterbi) walk over the tables; the literal
- *       "follow the best successor at each step" walk is kept as mode 1.
+ *       walk that takes the best successor at every step is kept as mode 1.
  *   R4  top-K order: value descending, then token id ascending.
  *   R5  Viterbi ties: the smallest predecessor rank wins; at the end the
  *       smallest final rank wins. Greedy ties: the smallest rank wins.
@@ -55,7 +55,7 @@ static double bf16_to_f64(uint16_t bits)
 }
 
 /* U[n*V + v] = sum_i W[v, i] * H[n, i]: the lm_head logit of token v at
- * position n ("DFlash's own logit", U_t(b) of the S_t equation). */
+ * position n (the drafter's own logit, U_t(b) of the S_t equation). */
 void oracle_logits(const uint16_t *W, const uint16_t *H, int64_t V, int64_t d, int64_t N,
                    double *U, int nthreads)
 {
@@ -324,8 +324,8 @@ int oracle_max_threads(void)
 /* ---------------------------------------------------------------------------
  * Sampling (temperature T > 0). Blog "DFlash 2: Keep Drafting Parallel",
  * section "A Lightweight Path Selector": sampling draws from the same pair
- * scores, and rejection sampling at verification restores the exact target
- * distribution. Readings (listed in the design notes):
+ * scores, and verification by rejection sampling leaves the output distributed
+ * exactly as the target's. Readings (listed in the design notes):
  *   S1  the draft distribution at step t is the softmax over the K candidate
  *       ranks of P[t, prev, .] / T, prev = the rank chosen at t-1 (row 0 at
  *       t = 0), and the step draws by inverting its CDF in rank order with a
@@ -444,8 +444,8 @@ int oracle_verify_rejection(int L, int K, int64_t V, const int32_t *path, const 
  * k_{t,0} (.) x_t + k_{t,1} (.) x_{t-1}; each coefficient is a learned base
  * kernel plus a small correction computed from the current hidden state, and
  * every 16 channels share one correction; the first draft position reads the
- * last verified token's representation, each later one its predecessor's; the
- * convolution is block-local and stateless. Readings (listed in the design
+ * last verified token's representation, each later one its predecessor's; nothing
+ * carries over from one block to the next. Readings (listed in the design
  * notes):
  *   C1  a block is S rows: the last verified token's representation, then the
  *       draft positions; row 0 has no predecessor (x_{-1} = 0);

@@ -1,10 +1,10 @@
 // Greedy accept check of a draft path against the target's argmax tokens.
 //
-// Blog "DFlash 2: Keep Drafting Parallel" (introduction): the target model
-// verifies the whole drafted block in one forward pass; good guesses are kept
-// and bad ones thrown away. With greedy decoding the kept guesses are the
-// longest prefix of the path that equals the target's own argmax tokens, and
-// the target contributes one more token (its argmax after that prefix).
+// Blog "DFlash 2: Keep Drafting Parallel" (introduction): one pass of the
+// target checks a whole drafted block, retaining the drafts it agrees with.
+// Under greedy decoding those are the longest prefix of the path equal to the
+// target's own argmax tokens, and the target adds one token of its own (its
+// argmax after that prefix).
 // One warp per sequence: lane t compares position t, a ballot finds the first
 // mismatch.
 #include <cooperative_groups.h>
@@ -53,14 +53,15 @@ cudaError_t launch_verify(const int32_t *path, const int32_t *target, int B, int
 }  // namespace dfl
 
 // Rejection-sampling verification of a sampled draft (blog "DFlash 2: Keep
-// Drafting Parallel", section "A Lightweight Path Selector": rejection
-// sampling restores the exact target distribution). Draft token x_t is kept
-// when u_acc_t < min(1, p_t(x_t) / q_t(x_t)), i.e. u_acc_t * q_t(x_t) <
-// p_t(x_t) (a product of two floats, exact in double precision); at the first
-// rejection the emitted token is drawn from the residual max(0, p_t - q_t)
-// (q_t is zero off the K candidates), normalised, by inverting its CDF in
-// vocabulary order with u_res; when all L drafts are kept the bonus token is
-// drawn from p_L. A residual with no mass at all falls back to p_t itself.
+// Drafting Parallel", section "A Lightweight Path Selector": verified by
+// rejection sampling, the output follows the target's distribution exactly).
+// Draft token x_t is kept when u_acc_t < min(1, p_t(x_t) / q_t(x_t)), i.e.
+// u_acc_t * q_t(x_t) < p_t(x_t) (a product of two floats, exact in double
+// precision); at the first rejection the emitted token is drawn from the
+// residual max(0, p_t - q_t) (q_t is zero off the K candidates), normalised,
+// by inverting its CDF in vocabulary order with u_res; when all L drafts are
+// kept the bonus token is drawn from p_L. A residual with no mass at all falls
+// back to p_t itself.
 //
 // The draw reads one whole vocabulary row per sequence: a thread-block
 // cluster of C CTAs per sequence shares it (C from 1 to 16, chosen by the

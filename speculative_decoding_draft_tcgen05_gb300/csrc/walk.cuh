@@ -7,8 +7,8 @@
 // delta_t(j) = max_i delta_{t-1}(i) + S_t(i, j), the smallest rank i winning
 // ties; the path ends at the best final rank (smallest on ties) and is read
 // back through the back-pointers. Greedy walk: from x0, the best successor at
-// every step (smallest rank on ties). Sampling walk (the pages: "sampling
-// draws from the same scores"): at every step the next rank is drawn from
+// every step (smallest rank on ties). Sampling walk (the pages draw samples
+// from the same pair scores): at every step the next rank is drawn from
 // softmax(S_t(prev, .) / T) over the K candidates by inverting its CDF in rank
 // order with a given uniform u_t; the distribution is written out for the
 // rejection-sampling verifier. One warp, lane j = candidate rank j.

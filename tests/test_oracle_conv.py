@@ -65,9 +65,9 @@ def test_correction_shared_by_16_channels_and_taken_from_the_current_row():
 
 
 def test_parameter_count_matches_the_pages():
-    """Base [2, d] + Wc [2 d/16, d] per convolution, one before and one after
-    each attention and feed-forward sublayer of the five-layer drafter (20 in
-    all), at the Qwen3-4B width d = 2560: the pages' 16.5M added parameters."""
+    """Base [2, d] + Wc [2 d/16, d] per convolution, one in front of and one
+    behind every attention and every feed-forward sublayer of the five-layer
+    drafter (20 in all), at the Qwen3-4B width d = 2560: the pages' 16.5M added parameters."""
     d = 2560
     per_conv = 2 * d + 2 * (d // 16) * d
     total = 5 * 2 * 2 * per_conv
