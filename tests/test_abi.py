@@ -49,3 +49,13 @@ def test_no_cpu_fallback_in_product_package():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import oracle|from oracle)", src, flags=re.M), f
                 assert "liboracle" not in src, f
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library the binding raises; it never falls back to
+    anything else."""
+    import speculative_decoding_draft_tcgen05_gb300 as pkg
+    monkeypatch.setattr(pkg, "LIB_PATH", str(tmp_path / "libdflash_select.so"))
+    monkeypatch.setattr(pkg, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        pkg.lib()
