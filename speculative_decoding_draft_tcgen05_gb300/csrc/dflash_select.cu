@@ -646,7 +646,14 @@ static dflash_status launch_lmhead(dflash_select_ctx *c, const void *hidden, con
     lp.thr_g = c->thr_g;
     lp.tmax = c->tmax;
     lp.epoch = ++c->epoch;
-    if (lp.epoch == 0) lp.epoch = ++c->epoch;  // 0 is the value of the zeroed workspace
+    if (lp.epoch == 0) {
+        // The counter wrapped: clear the tagged maxima (tag 0, never current),
+        // so that no entry left from 2^32 runs ago can carry the new epoch.
+        const size_t row = static_cast<size_t>(c->cfg.max_batch) * c->cfg.L * 8;
+        CUDA_TRY(cudaMemsetAsync(c->tmax, 0, static_cast<size_t>(c->num_sms) * row, s));
+        CUDA_TRY(cudaMemsetAsync(c->pmax, 0, static_cast<size_t>(kPilotMaxTiles) * row, s));
+        lp.epoch = ++c->epoch;
+    }
     lp.err = c->err;
 
     prof_begin(c, 0, s);
@@ -752,7 +759,12 @@ static dflash_status launch_tail(dflash_select_ctx *c, const int32_t *anchor, in
         dd.K = c->cfg.K;
         dd.R = c->R;
         dd.epoch = ++c->dd_epoch;
-        if (dd.epoch == 0) dd.epoch = ++c->dd_epoch;  // 0 is the zeroed table's mark
+        if (dd.epoch == 0) {
+            // The counter wrapped: marks of older epochs would outrank the new
+            // ones under atomicMax, so the table is cleared (mark 0) first.
+            CUDA_TRY(cudaMemsetAsync(c->dd_tab, 0, static_cast<size_t>(c->cfg.V) * 8, s));
+            dd.epoch = ++c->dd_epoch;
+        }
     }
     int slot = 1;  // profiling slots are filled in launch order
     prof_begin(c, slot, s);
@@ -1017,7 +1029,10 @@ dflash_status dflash_select_step_host(dflash_select_handle h, const void *hidden
     CUDA_TRY(cudaMemcpyAsync(c->st_hidden, hidden_host, nb * L * c->cfg.d * 2, cudaMemcpyHostToDevice, s));
     // the walkers write the results, a copy of the error word and a flag per
     // sequence straight into the mapped block
-    const uint32_t step = ++c->host_step;
+    // never 0, the value the flags start with: after the counter wraps, a
+    // sequence slot not used before must not read as finished
+    if (++c->host_step == 0) c->host_step = 1;
+    const uint32_t step = c->host_step;
     c->hs_done = c->hd_done;
     c->hs_err_snap = c->hd_err;
     c->hs_step = step;
